@@ -1,0 +1,321 @@
+"""fp64 CPU oracle for speculative-decoding verify attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module.  The library under
+``speculative_decoding_verify_kv_gb300`` never imports it, and this module
+imports nothing from the library: the two share no code.
+
+What it computes (plain definition, float64, no blocking or fusion):
+
+For sequence s, local draft row j and query head h of a verify launch:
+
+1. KV head ``kvh = h // G`` with ``G = H / KVH`` (contiguous head groups).
+2. The KV span holds ``L = ctx + n`` tokens; the draft rows' own K/V sit at
+   positions ``ctx .. ctx+n-1`` of the same cache.
+3. Visible set ``V = {0..ctx-1} ∪ {ctx + a : a == j or a is an ancestor of j}``.
+   A chain (and a one-row direct / AR row) has ``parent[j] = j-1``; a tree
+   suffix follows its parent array to -1.  Sources: lucebox PR #686 "retain
+   speculation during paged prefill", section "State and commit invariants"
+   (tree rows carry ancestry metadata over a fixed-width suffix; prompt and AR
+   rows stay positioned causal reads) and section "Mechanism" (the
+   [prefill][direct/AR][tree] lowering).
+4. Decode storage exactly to float64: bf16 by bit shift, fp16 by explicit bit
+   decode, Q8_0 as ``double(fp16 scale) * double(int8 code)`` per 32-element
+   block (hipfire PR #695, alpineQ comments: the ``attention_flash_q8_0_*``
+   kernels read a Q8 KV cache; Q8_0's 32-element blocks with one fp16 scale).
+5. ``z_t = scale * sum_d q_d k_{t,d}``, ``M = max z``, ``w_t = exp(z_t - M)``,
+   ``l = sum w``, ``O = sum_t w_t v_t / l``, ``LSE = M + ln l``.
+
+The split variant follows the FA2 split-KV design of hipfire PR #817
+("speed up long-context DFlash verify 13.4% with FA2 split-KV", sections
+"Summary" and "Performance": S chunks write online-softmax partials that a
+merge pass combines): each chunk yields ``(m_s, l_s, acc_s)`` in float64 and
+the merge takes ``M = max m_s``, ``l = sum e^{m_s-M} l_s``,
+``O = sum e^{m_s-M} acc_s / l``.  The chunk rule depends only on the
+sequence's own span L and the split count S, never on what else shares the
+launch (lucebox PR #686, section "Correctness failure found during
+qualification": the 1,024-token partition boundary).
+
+Parity status: every function below is pinned by ``tests/test_oracle.py``
+(brute force, closed forms, library special cases, invariants and hand-worked
+fixtures under ``tests/golden/``).
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import numpy as np
+
+PAGE = 16
+Q8_BLOCK = 32
+Q8_BLOCK_BYTES = 34
+
+
+# ---------------------------------------------------------------------------
+# Exact decoding of the storage formats.
+
+def decode_bf16(bits) -> np.ndarray:
+    """bf16 bits -> float64: the bf16 pattern is the top half of an fp32."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    with np.errstate(invalid="ignore"):
+        return b.view(np.float32).astype(np.float64)
+
+
+def decode_fp16(bits) -> np.ndarray:
+    """IEEE binary16 bits -> float64, decoded field by field."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    sign = np.where((b >> 15) & 1, -1.0, 1.0)
+    exp = (b >> 10) & 0x1F
+    man = (b & 0x3FF).astype(np.float64)
+    normal = sign * (1024.0 + man) * np.exp2(exp.astype(np.float64) - 25.0)
+    subnormal = sign * man * 2.0 ** -24
+    special = np.where(man == 0, sign * np.inf, np.nan)
+    return np.where(exp == 0, subnormal, np.where(exp == 31, special, normal))
+
+
+def dequant_q8_0(raw) -> np.ndarray:
+    """Q8_0 rows ``[..., nb*34]`` (uint8) -> float64 ``[..., nb*32]``.
+
+    Each 34-byte block is a little-endian fp16 scale d followed by 32 int8
+    codes q; element i of the block is d * q[i].
+    """
+    raw = np.asarray(raw, dtype=np.uint8)
+    nb = raw.shape[-1] // Q8_BLOCK_BYTES
+    blk = raw.reshape(raw.shape[:-1] + (nb, Q8_BLOCK_BYTES))
+    sbits = blk[..., 0].astype(np.uint16) | (blk[..., 1].astype(np.uint16) << 8)
+    d = decode_fp16(sbits)
+    q = blk[..., 2:].copy().view(np.int8).astype(np.float64)
+    return (d[..., None] * q).reshape(raw.shape[:-1] + (nb * Q8_BLOCK,))
+
+
+def decode_rows(rows, kv_dtype: str) -> np.ndarray:
+    if kv_dtype == "f32":
+        return np.asarray(rows, dtype=np.float32).astype(np.float64)
+    if kv_dtype == "bf16":
+        return decode_bf16(rows)
+    if kv_dtype == "q8_0":
+        return dequant_q8_0(rows)
+    raise ValueError(kv_dtype)
+
+
+def decode_q(q, q_dtype: str) -> np.ndarray:
+    return decode_rows(q, q_dtype)
+
+
+# ---------------------------------------------------------------------------
+# Row map, masks and KV addressing.
+
+def ancestors(parent_local, j: int) -> list[int]:
+    """Ancestors of draft node j: follow parent links until -1."""
+    out = []
+    p = int(parent_local[j])
+    while p >= 0:
+        if p >= j or p in out:
+            raise ValueError(f"parent array is not topological at node {j}")
+        out.append(p)
+        p = int(parent_local[p])
+    return out
+
+
+def row_masks(n: int, kind: int, parent_local) -> list[int]:
+    """Per local row j: bit a set iff draft position a is visible to row j
+    (a == j or a is an ancestor).  kind 0 = chain / direct, 1 = tree."""
+    masks = []
+    for j in range(n):
+        if kind == 0:
+            vis = range(j + 1)
+        else:
+            vis = [j] + ancestors(parent_local, j)
+        m = 0
+        for a in vis:
+            m |= 1 << a
+        masks.append(m)
+    return masks
+
+
+def row_map(cu_rows, parent, seq_kind, mode: str):
+    """Global row -> (sequence, ancestor mask).  Returns int32 row_seq and
+    uint32 masks (rows with n > 32 are not representable and rejected)."""
+    cu = np.asarray(cu_rows)
+    total = int(cu[-1])
+    row_seq = np.empty(total, dtype=np.int32)
+    masks = np.empty(total, dtype=np.uint32)
+    for s in range(len(cu) - 1):
+        lo, hi = int(cu[s]), int(cu[s + 1])
+        if hi - lo > 32:
+            raise ValueError("at most 32 rows per sequence")
+        kind = seq_kind_of(s, seq_kind, mode)
+        pl = None if parent is None else np.asarray(parent[lo:hi])
+        for j, m in enumerate(row_masks(hi - lo, kind, pl)):
+            row_seq[lo + j] = s
+            masks[lo + j] = m
+    return row_seq, masks
+
+
+def seq_kind_of(s: int, seq_kind, mode: str) -> int:
+    if mode == "chain":
+        return 0
+    if mode == "tree":
+        return 1
+    return int(seq_kind[s])
+
+
+def visible_positions(ctx: int, n: int, kind: int, parent_local, j: int) -> np.ndarray:
+    """Sorted KV positions visible to local row j."""
+    if kind == 0:
+        drafts = list(range(j + 1))
+    else:
+        drafts = sorted([j] + ancestors(parent_local, j))
+    return np.concatenate([np.arange(ctx, dtype=np.int64),
+                           np.asarray([ctx + a for a in drafts], dtype=np.int64)])
+
+
+def gather_index(s: int, kvh: int, t, *, page_size: int, capacity: int,
+                 num_kv_heads: int, block_table=None):
+    """Physical row of token t of sequence s, KV head kvh, counted in rows of
+    the cache array: contiguous ``[seq][KVH][capacity]`` or paged
+    ``[block][KVH][16]`` (page ``block_table[s][t // 16]``, slot ``t % 16``)."""
+    t = np.asarray(t, dtype=np.int64)
+    if page_size == 0:
+        return (s * num_kv_heads + kvh) * capacity + t
+    blk = np.asarray(block_table)[s, t // PAGE].astype(np.int64)
+    return (blk * num_kv_heads + kvh) * PAGE + t % PAGE
+
+
+def kv_rows(cache, s: int, kvh: int, L: int, *, page_size: int, capacity: int,
+            num_kv_heads: int, block_table=None) -> np.ndarray:
+    """Storage rows of tokens 0..L-1 for (s, kvh)."""
+    flat = np.asarray(cache).reshape(-1, np.asarray(cache).shape[-1])
+    idx = gather_index(s, kvh, np.arange(L), page_size=page_size, capacity=capacity,
+                       num_kv_heads=num_kv_heads, block_table=block_table)
+    return flat[idx]
+
+
+def kv_head_of(h: int, G: int) -> int:
+    """Grouped-query mapping: query heads come in contiguous groups of G per
+    KV head (H24/KV4 gives heads 0..5 -> KV head 0, 6..11 -> 1, ...)."""
+    return h // G
+
+
+# ---------------------------------------------------------------------------
+# Attention of one row over its visible set.
+
+def attend(q, K, V, scale: float):
+    """Softmax attention of one query over keys K [T, D] and values V [T, D]:
+    returns (o [D], lse, weights [T])."""
+    z = scale * np.einsum("td,d->t", K, q)
+    M = z.max()
+    w = np.exp(z - M)
+    l = w.sum()
+    o = np.einsum("t,td->d", w, V) / l
+    return o, M + math.log(l), w / l
+
+
+def split_ranges(L: int, S: int) -> list[tuple[int, int]]:
+    """Chunk rule of the split-KV pass: chunk = ceil(L / S) rounded up to a
+    multiple of 16 tokens; chunk s covers [s*chunk, min((s+1)*chunk, L)) and
+    may be empty.  Depends only on this sequence's L and S."""
+    per_split = -(-L // S)                      # ceil(L / S)
+    chunk = -(-per_split // PAGE) * PAGE        # rounded up to 16 tokens
+    return [(min(s * chunk, L), min((s + 1) * chunk, L)) for s in range(S)]
+
+
+def partial(q, K, V, pos, lo: int, hi: int, scale: float):
+    """Online-softmax partial of one chunk: (m, l, acc) over the visible
+    positions inside [lo, hi); an empty chunk gives (-inf, 0, 0)."""
+    sel = (pos >= lo) & (pos < hi)
+    if not sel.any():
+        return -math.inf, 0.0, np.zeros(K.shape[1])
+    Kc, Vc = K[pos[sel]], V[pos[sel]]
+    z = scale * np.einsum("td,d->t", Kc, q)
+    m = z.max()
+    w = np.exp(z - m)
+    return m, w.sum(), np.einsum("t,td->d", w, Vc)
+
+
+def merge(parts):
+    """Combine chunk partials in ascending chunk order."""
+    live = [p for p in parts if p[1] > 0]
+    M = max(p[0] for p in live)
+    l = sum(math.exp(m - M) * ls for m, ls, _ in live)
+    acc = sum(math.exp(m - M) * a for m, _, a in live)
+    return acc / l, M + math.log(l)
+
+
+# ---------------------------------------------------------------------------
+# The whole verify launch.
+
+def verify_attention(q, k, v, *, kv_dtype: str, q_dtype: str, num_heads: int,
+                     num_kv_heads: int, head_dim: int, ctx_len, cu_rows,
+                     parent=None, seq_kind=None, mode: str = "chain",
+                     page_size: int = 0, capacity: int = 0, block_table=None,
+                     scale: float = 0.0, num_splits: Optional[int] = None,
+                     rows: Optional[list] = None, heads: Optional[list] = None,
+                     return_weights: bool = False):
+    """Verify attention for every (row, head) (or the ``rows`` x ``heads``
+    subset).  Returns O [total_rows, H, D] and LSE [total_rows, H] in float64
+    (entries outside the subset are NaN).  ``num_splits=None`` is the
+    unsplit definition; an integer S takes the split-and-merge route."""
+    H, KVH, D = num_heads, num_kv_heads, head_dim
+    if H % KVH:
+        raise ValueError("H must be a multiple of KVH")
+    G = H // KVH
+    if scale == 0.0:
+        scale = 1.0 / math.sqrt(D)
+    cu = np.asarray(cu_rows, dtype=np.int64)
+    ctx_len = np.asarray(ctx_len, dtype=np.int64)
+    total = int(cu[-1])
+    O = np.full((total, H, D), np.nan)
+    LSE = np.full((total, H), np.nan)
+    W = {}
+    rowset = set(range(total)) if rows is None else set(int(r) for r in rows)
+    headset = list(range(H)) if heads is None else [int(h) for h in heads]
+    Q = decode_q(np.asarray(q).reshape(total, H, -1), q_dtype) if total else None
+    for s in range(len(ctx_len)):
+        lo, hi = int(cu[s]), int(cu[s + 1])
+        n = hi - lo
+        todo = [r for r in range(lo, hi) if r in rowset]
+        if not todo:
+            continue
+        ctx = int(ctx_len[s])
+        L = ctx + n
+        kind = seq_kind_of(s, seq_kind, mode)
+        pl = None if parent is None else np.asarray(parent)[lo:hi]
+        for kvh in sorted(set(kv_head_of(h, G) for h in headset)):
+            K = decode_rows(kv_rows(k, s, kvh, L, page_size=page_size, capacity=capacity,
+                                    num_kv_heads=KVH, block_table=block_table), kv_dtype)
+            V = decode_rows(kv_rows(v, s, kvh, L, page_size=page_size, capacity=capacity,
+                                    num_kv_heads=KVH, block_table=block_table), kv_dtype)
+            for r in todo:
+                j = r - lo
+                pos = visible_positions(ctx, n, kind, pl, j)
+                for h in headset:
+                    if kv_head_of(h, G) != kvh:
+                        continue
+                    qv = Q[r, h]
+                    if num_splits is None:
+                        o, lse, w = attend(qv, K[pos], V[pos], scale)
+                        if return_weights:
+                            W[(r, h)] = (pos, w)
+                    else:
+                        parts = [partial(qv, K, V, pos, a, b, scale)
+                                 for a, b in split_ranges(L, int(num_splits))]
+                        o, lse = merge(parts)
+                    O[r, h] = o
+                    LSE[r, h] = lse
+    if return_weights:
+        return O, LSE, W
+    return O, LSE
+
+
+def verify_case(case, **kw):
+    """Convenience wrapper taking a case object with the storage fields of
+    the synthetic generator (duck-typed; no import of the generator)."""
+    return verify_attention(
+        case.q, case.k, case.v, kv_dtype=case.kv_dtype, q_dtype=case.q_dtype,
+        num_heads=case.num_heads, num_kv_heads=case.num_kv_heads,
+        head_dim=case.head_dim, ctx_len=case.ctx_len, cu_rows=case.cu_rows,
+        parent=case.parent, seq_kind=case.seq_kind, mode=case.mode,
+        page_size=case.page_size, capacity=case.capacity,
+        block_table=case.block_table, scale=case.scale, **kw)
