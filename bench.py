@@ -1,0 +1,461 @@
+"""Verify-attention benchmark (one JSON line on rank 0).
+
+Workload (one step = one verify call, partial + merge): the long-context Q8
+verify shape — 1 sequence, B=16 chain rows, H24/KV4/D256, Q8_0 cache, bf16
+Q, context 32,768, split-KV S=8 — on synthetic seeded inputs.  Contexts
+8,192 and 20,676 are measured too and reported under ``contexts``.
+
+Timing: W eager warm-up calls, then EXACTLY K calls replayed from CUDA
+graphs, bracketed by a barrier and cudaDeviceSynchronize, timed with CUDA
+events on the launching stream; max over ranks.  The KV cache rotates
+through enough copies (>= 3x the L2 size) that every call reads from HBM.
+The library records per-kernel CUDA events inside the same graphs; the
+partial kernel's mean duration in the timed region gives the roofline line.
+
+``--impl reference`` times the fp64 CPU oracle (the reference arm) on a
+bounded sample of the same workload.
+
+Multi-GPU: the path does not shard inside one call; N ranks run N
+independent replicas ("weak" scaling) and ``value`` sums their KV bytes
+over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verify-attn us/call and KV-read GB/s (% HBM peak), B=16 H24/KV4/D256, 8K-32K"
+UNIT = "GB/s"
+HEADLINE_CTX = 32768
+OTHER_CTX = [8192, 20676]
+SPLITS = 8
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample-kv-heads", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "cuda-cores"])
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline).
+
+def oracle_sample(case, kv_heads: int):
+    """Run the oracle on every (row, head) of the first ``kv_heads`` KV heads
+    of the case; returns (seconds, fraction of the call's KV bytes)."""
+    import oracle
+    G = case.num_heads // case.num_kv_heads
+    heads = list(range(kv_heads * G))
+    t = time.perf_counter()
+    oracle.verify_case(case, heads=heads)
+    dt = time.perf_counter() - t
+    return dt, kv_heads / case.num_kv_heads
+
+
+def cpu_baseline(case, kv_heads: int):
+    dt, frac = oracle_sample(case, kv_heads)
+    gbs = case.kv_bytes * frac / dt / 1e9
+    return {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"fp64 numpy oracle, single thread: all 16 rows x {kv_heads * 6} query heads "
+                      f"({kv_heads} of 4 KV heads) of one ctx-{case.ctx_len[0]} call, "
+                      f"{dt:.2f} s; GB/s = that share of the call's KV bytes / time"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup_cpu()
+    if rank != 0:
+        return
+    import synthetic as sy
+    case = sy.long_q8(ctx=HEADLINE_CTX, num_splits=SPLITS)
+    kvh = 1
+    for _ in range(args.warmup):
+        oracle_sample(case, kvh)
+    times = []
+    for _ in range(args.steps):
+        dt, frac = oracle_sample(case, kvh)
+        times.append(dt)
+    total = sum(times)
+    gbs = case.kv_bytes * frac * len(times) / total / 1e9
+    ms = total / len(times) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"long-context Q8 verify: 1 seq, B=16 chain, H24/KV4/D256, "
+                                   f"Q8_0 KV, ctx {HEADLINE_CTX}, S={SPLITS}",
+                       "sample": "each step: the fp64 oracle on 1 of 4 KV heads (16 rows x 6 heads)"},
+            "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "1 of 4 KV heads of one ctx-32768 call per step"},
+            "e2e": {"value": gbs, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def dist_setup_cpu():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    return world, rank, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region.
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.idx = gpu_id
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() in ("active", "1"):
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm.
+
+class Bench:
+    """Device-resident workload with rotating KV copies and the library calls
+    captured in CUDA graphs."""
+
+    def __init__(self, case, flags, l2_bytes):
+        import torch
+
+        import speculative_decoding_verify_kv_gb300 as va
+        self.va = va
+        self.case = case
+        self.p, self.kv, self.mode = va.upload(case, "cuda", flags=flags)
+        kv_tensor_bytes = self.kv.k.numel() * self.kv.k.element_size() * 2
+        self.copies = max(2, -(-3 * l2_bytes // kv_tensor_bytes))
+        self.kvs = [self.kv]
+        for _ in range(self.copies - 1):
+            k2, v2 = self.kv.k.clone(), self.kv.v.clone()
+            self.kvs.append(va.KV(self.kv.dtype, self.kv.num_kv_heads, self.kv.head_dim, k2, v2,
+                                  page_size=self.kv.page_size, capacity=self.kv.capacity,
+                                  block_table=self.kv.block_table,
+                                  max_blocks_per_seq=self.kv.max_blocks_per_seq,
+                                  num_blocks=self.kv.num_blocks))
+        dev = "cuda"
+        self.ws = va.alloc_workspace(self.p, self.kv, dev)
+        self.o = torch.empty((case.total_rows, case.num_heads, case.head_dim),
+                             dtype=torch.float32, device=dev)
+        self.lse = torch.empty((case.total_rows, case.num_heads), dtype=torch.float32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.Stream()
+        self.plan = va.plan(self.p, self.kv, self.mode)
+
+    def call(self, i):
+        self.va.verify_attn(self.p, self.kvs[i % self.copies], self.mode, ws=self.ws, o=self.o,
+                            lse=self.lse, status=self.status, stream=self.stream)
+
+    def capture(self, calls_per_graph):
+        import torch
+        torch.cuda.synchronize()
+        self.singles = []
+        for i in range(self.copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                self.call(i)
+            self.singles.append(g)
+        self.block_calls = calls_per_graph
+        # create the library's timing events eagerly, then capture with them
+        self.va.timing_enable(True)
+        for i in range(calls_per_graph):
+            self.call(i)
+        torch.cuda.synchronize()
+        self.va.timing_enable(True)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for i in range(calls_per_graph):
+                self.call(i)
+        self.va.timing_enable(False)
+        self.block = g
+        torch.cuda.synchronize()
+
+    def replay(self, calls):
+        nb, rem = divmod(calls, self.block_calls)
+        for _ in range(nb):
+            self.block.replay()
+        for i in range(rem):
+            self.singles[i % self.copies].replay()
+
+    def timed(self, calls, world):
+        import torch
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            self.replay(calls)
+            e1.record(self.stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return e0.elapsed_time(e1)
+
+
+def e2e_measure(case, steps, warmup, flags):
+    """The same call through the public API with HOST buffers: every step
+    copies the inputs from pinned host memory, calls the library and reads
+    O and LSE back."""
+    import torch
+
+    import speculative_decoding_verify_kv_gb300 as va
+    p, kv, mode = va.upload(case, "cuda", flags=flags)
+    host = {}
+    for name, t in [("q", p.q), ("k", kv.k), ("v", kv.v), ("cu_rows", p.cu_rows),
+                    ("ctx_len", p.ctx_len), ("parent", p.parent), ("seq_kind", p.seq_kind)]:
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t.cpu())
+        host[name] = (h, t)
+    o_h = torch.empty((case.total_rows, case.num_heads, case.head_dim), dtype=torch.float32,
+                      pin_memory=True)
+    l_h = torch.empty((case.total_rows, case.num_heads), dtype=torch.float32, pin_memory=True)
+    ws = va.alloc_workspace(p, kv, "cuda")
+    o = torch.empty(o_h.shape, dtype=torch.float32, device="cuda")
+    lse = torch.empty(l_h.shape, dtype=torch.float32, device="cuda")
+    st = torch.cuda.Stream()
+    h2d = sum(h.numel() * h.element_size() for h, _ in host.values())
+    d2h = o_h.numel() * 4 + l_h.numel() * 4
+
+    def step():
+        for h, d in host.values():
+            d.copy_(h, non_blocking=True)
+        va.verify_attn(p, kv, mode, ws=ws, o=o, lse=lse, stream=st)
+        o_h.copy_(o, non_blocking=True)
+        l_h.copy_(lse, non_blocking=True)
+
+    with torch.cuda.stream(st):
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(steps):
+            step()
+        e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": case.kv_bytes / (ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+
+
+def run_ours(args):
+    import torch
+
+    import speculative_decoding_verify_kv_gb300 as va
+    import synthetic as sy
+    world, rank, local = dist_setup()
+    assert torch.cuda.is_available(), "bench needs a GPU"
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    flags = va.FLAG_CUDA_CORES if args.kernel == "cuda-cores" else 0
+    peak, peak_src = load_peaks()
+
+    # CPU baseline first (rank 0, N=1 only), before any GPU work.
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(sy.long_q8(ctx=HEADLINE_CTX, num_splits=SPLITS),
+                           args.cpu_sample_kv_heads)
+
+    case = sy.long_q8(ctx=HEADLINE_CTX, num_splits=SPLITS, seed=1003 + rank)
+    b = Bench(case, flags, l2)
+    for i in range(args.warmup):
+        b.call(i)
+    torch.cuda.synchronize()
+    assert int(b.status.item()) == 0, "device status set during warm-up"
+    calls_per_graph = 4 * b.copies
+    b.capture(calls_per_graph)
+
+    # Sustained load around the timed region so the clock sampler sees it.
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local)
+    sampler = ClockSampler(gpu_id) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    t_end = time.time() + 1.0
+    while time.time() < t_end:
+        b.replay(calls_per_graph * 8)
+        torch.cuda.synchronize()
+    ms = b.timed(args.steps, world)
+    partial_ms, merge_ms = va.timing_read(calls_per_graph)
+    t_end = time.time() + 0.5
+    while time.time() < t_end:
+        b.replay(calls_per_graph * 8)
+        torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    ms_max = max_over_ranks(ms, world)
+    per_call_ms = ms_max / args.steps
+    value = world * case.kv_bytes * args.steps / (ms_max * 1e-3) / 1e9
+    part_us = float(np.mean(partial_ms)) * 1e3 if partial_ms else None
+    merge_us = float(np.mean(merge_ms)) * 1e3 if merge_ms else None
+    achieved = case.kv_bytes / (part_us * 1e-6) / 1e9 if part_us else None
+
+    contexts = {}
+    for ctx in OTHER_CTX + [HEADLINE_CTX]:
+        if ctx == HEADLINE_CTX:
+            us = per_call_ms * 1e3
+            contexts[str(ctx)] = {"us_per_call": us,
+                                  "kv_gbs": case.kv_bytes / (us * 1e-6) / 1e9,
+                                  "partial_us": part_us, "merge_us": merge_us}
+            continue
+        c2 = sy.long_q8(ctx=ctx, num_splits=SPLITS, seed=1003 + rank)
+        b2 = Bench(c2, flags, l2)
+        for i in range(3):
+            b2.call(i)
+        b2.capture(4 * b2.copies)
+        n2 = max(4 * b2.copies, min(args.steps, 400))
+        ms2 = max_over_ranks(b2.timed(n2, world), world)
+        pm, mm = va.timing_read(4 * b2.copies)
+        us = ms2 / n2 * 1e3
+        contexts[str(ctx)] = {"us_per_call": us, "kv_gbs": c2.kv_bytes / (us * 1e-6) / 1e9,
+                              "partial_us": float(np.mean(pm)) * 1e3,
+                              "merge_us": float(np.mean(mm)) * 1e3}
+        del b2
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_measure(case, steps=max(3, min(args.steps, 50)), warmup=3, flags=flags)
+        e2e["value"] = world * e2e["value"] if world > 1 else e2e["value"]
+
+    if rank != 0:
+        return
+    kernel_name = "tensor-core partial" if b.plan["kernel"] == 1 else "CUDA-core partial"
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per_call_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if b.plan["kernel"] == 1 else "f32",
+        "data": "synthetic",
+        "config": {"workload": f"long-context Q8 verify: 1 seq, B=16 chain, H24/KV4/D256, Q8_0 "
+                               f"KV (bf16 Q), ctx {HEADLINE_CTX}, split-KV S={SPLITS}",
+                   "kv_bytes_per_call": case.kv_bytes, "seed": 1003,
+                   "l2": f"KV rotates through {b.copies} copies "
+                         f"({b.copies * b.kv.k.numel() * 2 / 2 ** 20:.0f} MiB >= 3x L2 "
+                         f"{l2 / 2 ** 20:.0f} MiB)",
+                   "launch": "CUDA graphs of library calls, "
+                             f"{calls_per_graph} calls per graph",
+                   "plan": b.plan},
+        "us_per_call": per_call_ms * 1e3,
+        "hbm_frac_call": value / world / peak,
+        "contexts": contexts,
+        "roofline": {"kernel": kernel_name, "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak if achieved else None,
+                     "traffic": None, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": case.kv_bytes},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,232 @@
+/*
+ * verify_attn.h — C ABI of the GB300 speculative-decoding verify-attention
+ * library (libverify_attn.so, sm_103a).
+ *
+ * The operation: a window of draft-token query rows per sequence attends over
+ * that sequence's KV cache.  Rows are causal along a chain, or follow a
+ * parent array for a fixed-width tree suffix; query heads are grouped over
+ * fewer KV heads; the cache is contiguous or paged in 16-token blocks and
+ * holds fp32, bf16 or Q8_0 rows.  The result per (row, head) is the softmax-
+ * weighted sum of the visible V rows (O) and the natural-log sum of the
+ * exponentiated scaled scores (LSE).
+ *
+ * Sources (the pages this library restates):
+ *   - hipfire PR #695 "perf(gfx11): optimize Qwen DFlash speculative verify":
+ *     section "Summary" (B=16 verify through batched flash attention), the
+ *     alpineQ comments (Q8 KV, one block reusing each KV fetch across several
+ *     verifier rows, the batched-partials layout and its reducer).
+ *   - hipfire PR #817 "speed up long-context DFlash verify 13.4% with FA2
+ *     split-KV": sections "Summary", "Default and admission policy" and
+ *     "Performance" (S8 split-KV partial + merge, caller-owned partial
+ *     workspace, fail-closed admission, S1 equal to the unsplit result).
+ *   - lucebox PR #686 "perf(qwen35): retain speculation during paged
+ *     prefill": sections "Mechanism", "State and commit invariants" and
+ *     "Correctness failure found during qualification" (direct rows and a
+ *     fixed-width tree suffix in one step over paged KV; tree ancestry
+ *     metadata; partitioning must not depend on what shares the launch).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named "device" are CUDA device memory owned by the caller;
+ *     the library never allocates, frees or keeps them past the call.
+ *   - Calls are asynchronous on the given CUDA stream (a cudaStream_t passed
+ *     as void*; NULL = legacy default stream).  Lengths and metadata are read
+ *     on the device, so the host never synchronises.
+ *   - Host-checkable errors return a status and launch nothing.
+ *   - Data errors found on the device (bad parent, block id, row counts,
+ *     context beyond capacity) OR a VA_DEV_* bit into *status (device word,
+ *     may be NULL) and the affected rows get NaN outputs.
+ */
+#ifndef VERIFY_ATTN_H
+#define VERIFY_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum va_status {
+  VA_OK = 0,
+  VA_ERR_INVALID_ARG = 1,         /* null pointer, negative size, bad enum */
+  VA_ERR_UNSUPPORTED = 2,         /* shape/dtype outside the supported set */
+  VA_ERR_ALIGNMENT = 3,           /* a pointer is not 16-byte aligned */
+  VA_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes < va_workspace_size() */
+  VA_ERR_CUDA = 5                 /* a CUDA runtime call or launch failed */
+} va_status;
+
+typedef enum va_dtype {
+  VA_F32 = 0,  /* IEEE fp32 */
+  VA_BF16 = 1, /* bfloat16 */
+  VA_Q8_0 = 2  /* 34-byte blocks: fp16 scale d (little endian), 32 int8 codes q; value d*q */
+} va_dtype;
+
+typedef enum va_mode {
+  VA_MODE_CHAIN = 0, /* every sequence is a chain: row j sees context + rows 0..j */
+  VA_MODE_TREE = 1,  /* every sequence is a tree over its rows (parent array) */
+  VA_MODE_MIXED = 2  /* per-sequence kind from seq_kind[] */
+} va_mode;
+
+/* Device status bits (OR-ed into *status). */
+#define VA_DEV_BAD_PARENT 0x1u   /* parent[j] not in [-1, j) */
+#define VA_DEV_BAD_BLOCK 0x2u    /* block_table entry outside [0, num_blocks) */
+#define VA_DEV_CTX_OVERFLOW 0x4u /* ctx + n exceeds capacity / the block table */
+#define VA_DEV_BAD_ROWS 0x8u     /* cu_rows not ascending, n > max_rows_per_seq, or total mismatch */
+#define VA_DEV_TIMEOUT 0x10u     /* a bounded pipeline wait gave up */
+
+/* Problem flags. */
+#define VA_FLAG_CUDA_CORES 0x1u /* run the CUDA-core (SIMT) partial kernel for any dtype */
+
+/*
+ * The KV cache.
+ *   contiguous (page_size == 0): k, v are [num_seqs][num_kv_heads][capacity][row];
+ *     capacity is a multiple of 16 tokens.
+ *   paged (page_size == 16): k, v are pools [num_blocks][num_kv_heads][16][row]
+ *     and token t of sequence s lives in block block_table[s*max_blocks_per_seq + t/16],
+ *     slot t%16 (lucebox PR #686, "Correctness failure found during
+ *     qualification": 16-token blocks).
+ *   row = head_dim fp32 / bf16 elements, or head_dim/32 Q8_0 blocks of 34 bytes.
+ *   The draft rows' own K/V sit at positions ctx .. ctx+n-1 of the same cache.
+ */
+typedef struct va_kv {
+  va_dtype dtype;
+  int32_t num_kv_heads;
+  int32_t head_dim;            /* 64, 128 or 256 */
+  const void *k;               /* device, 16-byte aligned */
+  const void *v;               /* device, 16-byte aligned */
+  int32_t page_size;           /* 0 or 16 */
+  int64_t capacity;            /* contiguous only: tokens per (sequence, KV head) */
+  const int32_t *block_table;  /* paged only: device [num_seqs][max_blocks_per_seq] */
+  int32_t max_blocks_per_seq;  /* paged only */
+  int32_t num_blocks;          /* paged only: blocks in the pool */
+} va_kv;
+
+/*
+ * The query side.
+ *   q: device [total_rows][num_heads][head_dim], fp32 or bf16 (bf16 for the
+ *      bf16 and Q8_0 caches; fp32 or bf16 for the fp32 cache).
+ *   Rows of sequence s are cu_rows[s] .. cu_rows[s+1]-1 (device array); row
+ *   j of a sequence sits at KV position ctx_len[s] + j.
+ *   parent: device [total_rows], the local index of each row's parent in its
+ *      own sequence, -1 for a node attached to the context; must satisfy
+ *      parent[j] < j.  Ignored for chain sequences (may be NULL in chain mode).
+ *   seq_kind: device [num_seqs], 0 = chain (a 1-row chain is a direct/AR
+ *      row), 1 = tree; read in VA_MODE_MIXED only.
+ *   Query head h reads KV head h / (num_heads / num_kv_heads).
+ *   scale: softmax scale; 0 selects 1/sqrt(head_dim).
+ *   num_splits: S >= 1.  Sequence s's span L = ctx + n is cut into S chunks
+ *      of ceil(L/S) tokens rounded up to 16; each chunk writes an fp32
+ *      online-softmax partial (possibly further cut into a fixed number of
+ *      sub-chunks chosen from S, num_kv_heads and the GPU's SM count only),
+ *      and a merge pass combines them in ascending order (hipfire PR #817,
+ *      "Summary" and "Performance").  No choice depends on the other
+ *      sequences of the launch, so a row's result depends only on its own
+ *      sequence (lucebox PR #686, "Correctness failure found during
+ *      qualification").
+ */
+typedef struct va_problem {
+  int32_t num_seqs;
+  int32_t num_heads;
+  va_dtype q_dtype;
+  const void *q;
+  const int32_t *cu_rows;
+  const int32_t *ctx_len;
+  const int32_t *parent;
+  const uint8_t *seq_kind;
+  int32_t total_rows;          /* host copy of cu_rows[num_seqs] */
+  int32_t max_rows_per_seq;    /* host bound on rows per sequence, 1..32 */
+  float scale;
+  int32_t num_splits;
+  uint32_t flags;              /* VA_FLAG_* */
+} va_problem;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int32_t va_version(void);
+
+/* Human-readable name of a status code; never NULL. */
+const char *va_status_string(va_status s);
+
+/*
+ * Bytes of device workspace a verify call needs for this problem: the fp32
+ * split partials (m, l and the unnormalised accumulator per split, row and
+ * head; hipfire PR #817 "Default and admission policy": the caller-owned
+ * partial workspace).  Returns 0 for an invalid problem.
+ */
+size_t va_workspace_size(const va_problem *p, const va_kv *kv);
+
+/*
+ * Host-only validation, no launch and no device access: the checks every
+ * verify call makes before launching (fail-closed admission as in hipfire
+ * PR #817 "Default and admission policy"; undersized workspace rejected).
+ */
+va_status va_validate(const va_problem *p, const va_kv *kv, int32_t mode, size_t ws_bytes);
+
+/*
+ * Verify attention.  o: device fp32 [total_rows][num_heads][head_dim];
+ * lse: device fp32 [total_rows][num_heads] (natural log).  ws: device
+ * workspace of at least va_workspace_size() bytes, 256-byte aligned;
+ * its contents need no initialisation and are overwritten.
+ *   verify_attn_chain: every sequence is a chain (also 1-row direct rows).
+ *   verify_attn_tree:  every sequence is a tree over its rows (parent required).
+ *   verify_attn_mixed: per-sequence chain or tree from seq_kind (lucebox PR
+ *                      #686 "Mechanism": direct rows and tree rows in one step).
+ */
+va_status verify_attn_chain(const va_problem *p, const va_kv *kv, void *ws, size_t ws_bytes,
+                            float *o, float *lse, uint32_t *status, void *stream);
+va_status verify_attn_tree(const va_problem *p, const va_kv *kv, void *ws, size_t ws_bytes,
+                           float *o, float *lse, uint32_t *status, void *stream);
+va_status verify_attn_mixed(const va_problem *p, const va_kv *kv, void *ws, size_t ws_bytes,
+                            float *o, float *lse, uint32_t *status, void *stream);
+
+/*
+ * Debug export of the row map and masks the kernels use: row_seq[r] is the
+ * sequence of global row r; anc_mask[r] has bit a set iff draft position a
+ * of that sequence is visible to row r (itself or an ancestor).  Device
+ * outputs of total_rows entries each.  (lucebox PR #686 "Correctness failure
+ * found during qualification": the compact row map and W8 topology checks.)
+ */
+va_status va_debug_row_map(const va_problem *p, int32_t mode, int32_t *row_seq,
+                           uint32_t *anc_mask, uint32_t *status, void *stream);
+
+/*
+ * Debug export of the KV gather the kernels use: phys_row[s*max_len + t] is
+ * the row of token t of sequence s, KV head kv_head, counted in rows of the
+ * k/v array (contiguous: (s*KVH+kvh)*capacity + t; paged:
+ * (block*KVH+kvh)*16 + t%16), or -1 for t >= ctx+n.  Device output of
+ * num_seqs*max_len int64.
+ */
+va_status va_debug_gather_index(const va_problem *p, const va_kv *kv, int32_t kv_head,
+                                int64_t max_len, int64_t *phys_row, uint32_t *status,
+                                void *stream);
+
+/* Plan details for a problem (which kernel runs, splits and sub-splits). */
+typedef struct va_plan_info {
+  int32_t kernel;          /* 0 = CUDA-core partial, 1 = tensor-core partial */
+  int32_t sub_splits;      /* P: sub-chunks per split */
+  int32_t slots;           /* S * P partial slots per (row, head) */
+  int32_t grid_x, grid_y, grid_z;
+  int32_t threads;
+  int32_t smem_bytes;
+} va_plan_info;
+
+va_status va_plan(const va_problem *p, const va_kv *kv, int32_t mode, va_plan_info *out);
+
+/*
+ * Optional per-kernel timing for benchmarks.  While enabled (on != 0),
+ * every verify call records CUDA events on its stream before the partial
+ * kernel, between the partial and merge kernels, and after the merge;
+ * enabling restarts at slot 0 (at most 4096 calls are kept).  Inside a
+ * stream capture the records become event nodes of the graph, so a replay
+ * refreshes them.  va_timing_read waits for the recorded events and writes
+ * each recorded call's partial and merge durations in milliseconds
+ * (host arrays of max_calls floats, either may be NULL).  Not thread-safe.
+ */
+va_status va_timing_enable(int32_t on);
+va_status va_timing_read(int32_t max_calls, float *partial_ms, float *merge_ms,
+                         int32_t *num_calls);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERIFY_ATTN_H */

@@ -1,0 +1,351 @@
+// Host side of the C ABI: validation (fail-closed, before any launch),
+// planning (kernel, splits, sub-chunks, grid), workspace sizing and the
+// launches on the caller's stream.
+//
+// Admission follows the fail-closed rule of hipfire PR #817 "Default and
+// admission policy": anything outside the supported set is rejected with a
+// status, never silently routed elsewhere; an undersized workspace is
+// rejected before launch.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <vector>
+
+#include "va_common.cuh"
+
+namespace va {
+cudaError_t launch_simt_partial(const Params& p, dim3 grid, cudaStream_t st);
+int simt_smem_bytes(int D);
+cudaError_t launch_merge(const Params& p, cudaStream_t st);
+cudaError_t launch_debug_row_map(const Params& p, int* row_seq, unsigned* anc, cudaStream_t st);
+cudaError_t launch_debug_gather(const Params& p, int kvh, long long max_len, long long* out,
+                                cudaStream_t st);
+
+constexpr int kSimtRowsPerBlock = 16;
+constexpr int kSimtThreadsPerBlock = 128;
+constexpr int kMinSubTokens = 256;
+constexpr int kMaxSubSplits = 16;
+
+static int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+static bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
+
+static int row_bytes_of(int dtype, int D) {
+  switch (dtype) {
+    case VA_F32: return 4 * D;
+    case VA_BF16: return 2 * D;
+    case VA_Q8_0: return D / kQ8Block * kQ8BlockBytes;
+  }
+  return 0;
+}
+
+// Checks that need no device access.  ws_bytes < 0 skips the workspace check.
+static va_status check(const va_problem* p, const va_kv* kv, int mode) {
+  if (!p || !kv) return VA_ERR_INVALID_ARG;
+  if (mode < VA_MODE_CHAIN || mode > VA_MODE_MIXED) return VA_ERR_INVALID_ARG;
+  if (p->num_seqs < 1 || p->num_heads < 1 || kv->num_kv_heads < 1) return VA_ERR_INVALID_ARG;
+  if (p->total_rows < 0 || p->num_splits < 1) return VA_ERR_INVALID_ARG;
+  if (p->max_rows_per_seq < 1) return VA_ERR_INVALID_ARG;
+  if (p->q_dtype < VA_F32 || p->q_dtype > VA_Q8_0) return VA_ERR_INVALID_ARG;
+  if (kv->dtype < VA_F32 || kv->dtype > VA_Q8_0) return VA_ERR_INVALID_ARG;
+  if (p->num_heads % kv->num_kv_heads) return VA_ERR_UNSUPPORTED;
+  int G = p->num_heads / kv->num_kv_heads;
+  if (G > 8) return VA_ERR_UNSUPPORTED;
+  if (kv->head_dim != 64 && kv->head_dim != 128 && kv->head_dim != 256) return VA_ERR_UNSUPPORTED;
+  if (p->max_rows_per_seq > 32) return VA_ERR_UNSUPPORTED;
+  if (p->num_splits > 256) return VA_ERR_UNSUPPORTED;
+  if (p->q_dtype == VA_Q8_0) return VA_ERR_UNSUPPORTED;
+  if (kv->dtype != VA_F32 && p->q_dtype != VA_BF16) return VA_ERR_UNSUPPORTED;
+  if (!(p->scale >= 0.f) || isinf(p->scale)) return VA_ERR_INVALID_ARG;
+  if (p->flags & ~(uint32_t)VA_FLAG_CUDA_CORES) return VA_ERR_INVALID_ARG;
+  if (!p->cu_rows || !p->ctx_len) return VA_ERR_INVALID_ARG;
+  if (p->total_rows > 0 && !p->q) return VA_ERR_INVALID_ARG;
+  if (mode != VA_MODE_CHAIN && !p->parent) return VA_ERR_INVALID_ARG;
+  if (mode == VA_MODE_MIXED && !p->seq_kind) return VA_ERR_INVALID_ARG;
+  if (!kv->k || !kv->v) return VA_ERR_INVALID_ARG;
+  if (kv->page_size == 0) {
+    if (kv->capacity < 1) return VA_ERR_INVALID_ARG;
+    if (kv->capacity % kPage) return VA_ERR_UNSUPPORTED;
+  } else if (kv->page_size == kPage) {
+    if (!kv->block_table || kv->max_blocks_per_seq < 1 || kv->num_blocks < 1)
+      return VA_ERR_INVALID_ARG;
+  } else {
+    return VA_ERR_UNSUPPORTED;
+  }
+  if (!aligned16(kv->k) || !aligned16(kv->v)) return VA_ERR_ALIGNMENT;
+  if (p->q && !aligned16(p->q)) return VA_ERR_ALIGNMENT;
+  return VA_OK;
+}
+
+struct Plan {
+  int kernel;  // 0 simt, 1 tensor-core
+  int P, slots, rows_per_block, row_blocks, threads, smem;
+  dim3 grid;
+};
+
+static Plan make_plan(const va_problem* p, const va_kv* kv) {
+  Plan pl;
+  const int G = p->num_heads / kv->num_kv_heads;
+  pl.kernel = 0;
+  pl.rows_per_block = kSimtRowsPerBlock;
+  pl.threads = kSimtThreadsPerBlock;
+  pl.smem = simt_smem_bytes(kv->head_dim);
+  // Sub-chunks per split from S, the KV head count and the SM count only:
+  // never from the other sequences of the launch.
+  const int target = 2 * sm_count();
+  int P = target / (p->num_splits * kv->num_kv_heads);
+  if (P < 1) P = 1;
+  if (P > kMaxSubSplits) P = kMaxSubSplits;
+  pl.P = P;
+  pl.slots = p->num_splits * P;
+  const int rows = p->max_rows_per_seq * G;
+  pl.row_blocks = (rows + pl.rows_per_block - 1) / pl.rows_per_block;
+  pl.grid = dim3((unsigned)(pl.slots * pl.row_blocks), (unsigned)kv->num_kv_heads,
+                 (unsigned)p->num_seqs);
+  return pl;
+}
+
+static size_t ws_bytes_for(const va_problem* p, const va_kv* kv, const Plan& pl) {
+  size_t items = (size_t)pl.slots * (size_t)p->total_rows * (size_t)p->num_heads;
+  size_t acc = items * (size_t)kv->head_dim * 4;
+  size_t ml = items * 2 * 4;
+  acc = (acc + 255) / 256 * 256;
+  ml = (ml + 255) / 256 * 256;
+  return acc + ml;
+}
+
+static Params make_params(const va_problem* p, const va_kv* kv, int mode, const Plan& pl,
+                          void* ws, float* o, float* lse, uint32_t* status) {
+  Params q;
+  memset(&q, 0, sizeof(q));
+  q.num_seqs = p->num_seqs;
+  q.H = p->num_heads;
+  q.KVH = kv->num_kv_heads;
+  q.G = p->num_heads / kv->num_kv_heads;
+  q.D = kv->head_dim;
+  q.total_rows = p->total_rows;
+  q.max_rows = p->max_rows_per_seq;
+  q.S = p->num_splits;
+  q.P = pl.P;
+  q.slots = pl.slots;
+  q.min_sub = kMinSubTokens;
+  q.mode = mode;
+  q.kv_dtype = kv->dtype;
+  q.q_dtype = p->q_dtype;
+  float sc = p->scale > 0.f ? p->scale : 1.0f / sqrtf((float)kv->head_dim);
+  q.scale_log2 = (float)((double)sc * 1.4426950408889634);
+  q.q = p->q;
+  q.cu_rows = p->cu_rows;
+  q.ctx_len = p->ctx_len;
+  q.parent = p->parent;
+  q.seq_kind = p->seq_kind;
+  q.k = kv->k;
+  q.v = kv->v;
+  q.page_size = kv->page_size;
+  q.capacity = kv->capacity;
+  q.block_table = kv->block_table;
+  q.max_blocks = kv->max_blocks_per_seq;
+  q.num_blocks = kv->num_blocks;
+  q.row_bytes = row_bytes_of(kv->dtype, kv->head_dim);
+  if (ws) {
+    size_t items = (size_t)pl.slots * (size_t)p->total_rows * (size_t)p->num_heads;
+    size_t acc = (items * (size_t)kv->head_dim * 4 + 255) / 256 * 256;
+    q.ws_acc = (float*)ws;
+    q.ws_ml = (float*)((char*)ws + acc);
+  }
+  q.o = o;
+  q.lse = lse;
+  q.status = (unsigned*)status;
+  q.rows_per_block = pl.rows_per_block;
+  q.row_blocks = pl.row_blocks;
+  return q;
+}
+
+// Optional per-kernel timing: while enabled, each verify call records CUDA
+// events around its partial and merge launches on the call's stream
+// (slots are reused from 0 each time timing is switched on; events made
+// during stream capture become event-record nodes of the graph).
+struct TimingSlot {
+  cudaEvent_t e[3];
+};
+static std::vector<TimingSlot> g_timing_slots;
+static bool g_timing_on = false;
+static int g_timing_next = 0;
+constexpr int kMaxTimingSlots = 4096;
+
+static TimingSlot* timing_slot() {
+  if (!g_timing_on || g_timing_next >= kMaxTimingSlots) return nullptr;
+  if (g_timing_next >= (int)g_timing_slots.size()) {
+    TimingSlot t;
+    for (int i = 0; i < 3; ++i)
+      if (cudaEventCreate(&t.e[i]) != cudaSuccess) return nullptr;
+    g_timing_slots.push_back(t);
+  }
+  return &g_timing_slots[g_timing_next++];
+}
+
+static va_status run(const va_problem* p, const va_kv* kv, int mode, void* ws, size_t ws_bytes,
+                     float* o, float* lse, uint32_t* status, void* stream) {
+  va_status st = check(p, kv, mode);
+  if (st != VA_OK) return st;
+  if (p->total_rows == 0) return VA_OK;
+  if (!o || !lse) return VA_ERR_INVALID_ARG;
+  if (!aligned16(o)) return VA_ERR_ALIGNMENT;
+  Plan pl = make_plan(p, kv);
+  size_t need = ws_bytes_for(p, kv, pl);
+  if (!ws || ws_bytes < need) return VA_ERR_WORKSPACE_TOO_SMALL;
+  if (((uintptr_t)ws & 255u) != 0) return VA_ERR_ALIGNMENT;
+  Params q = make_params(p, kv, mode, pl, ws, o, lse, status);
+  cudaStream_t cs = (cudaStream_t)stream;
+  TimingSlot* ts = timing_slot();
+  if (ts) cudaEventRecord(ts->e[0], cs);
+  cudaError_t e = launch_simt_partial(q, pl.grid, cs);
+  if (e != cudaSuccess) return VA_ERR_CUDA;
+  if (ts) cudaEventRecord(ts->e[1], cs);
+  e = launch_merge(q, cs);
+  if (e != cudaSuccess) return VA_ERR_CUDA;
+  if (ts) cudaEventRecord(ts->e[2], cs);
+  return VA_OK;
+}
+
+}  // namespace va
+
+using namespace va;
+
+extern "C" {
+
+int32_t va_version(void) { return 100; }
+
+const char* va_status_string(va_status s) {
+  switch (s) {
+    case VA_OK: return "ok";
+    case VA_ERR_INVALID_ARG: return "invalid argument";
+    case VA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case VA_ERR_ALIGNMENT: return "pointer not aligned";
+    case VA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case VA_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+size_t va_workspace_size(const va_problem* p, const va_kv* kv) {
+  if (check(p, kv, VA_MODE_CHAIN) != VA_OK && check(p, kv, VA_MODE_MIXED) != VA_OK) return 0;
+  Plan pl = make_plan(p, kv);
+  return ws_bytes_for(p, kv, pl);
+}
+
+va_status va_validate(const va_problem* p, const va_kv* kv, int32_t mode, size_t ws_bytes) {
+  va_status st = check(p, kv, mode);
+  if (st != VA_OK) return st;
+  if (p->total_rows == 0) return VA_OK;
+  Plan pl = make_plan(p, kv);
+  if (ws_bytes < ws_bytes_for(p, kv, pl)) return VA_ERR_WORKSPACE_TOO_SMALL;
+  return VA_OK;
+}
+
+va_status va_plan(const va_problem* p, const va_kv* kv, int32_t mode, va_plan_info* out) {
+  va_status st = check(p, kv, mode);
+  if (st != VA_OK) return st;
+  if (!out) return VA_ERR_INVALID_ARG;
+  Plan pl = make_plan(p, kv);
+  out->kernel = pl.kernel;
+  out->sub_splits = pl.P;
+  out->slots = pl.slots;
+  out->grid_x = (int32_t)pl.grid.x;
+  out->grid_y = (int32_t)pl.grid.y;
+  out->grid_z = (int32_t)pl.grid.z;
+  out->threads = pl.threads;
+  out->smem_bytes = pl.smem;
+  return VA_OK;
+}
+
+va_status va_timing_enable(int32_t on) {
+  g_timing_on = on != 0;
+  if (g_timing_on) g_timing_next = 0;
+  return VA_OK;
+}
+
+va_status va_timing_read(int32_t max_calls, float* partial_ms, float* merge_ms,
+                         int32_t* num_calls) {
+  if (!num_calls) return VA_ERR_INVALID_ARG;
+  int n = g_timing_next < max_calls ? g_timing_next : max_calls;
+  for (int i = 0; i < n; ++i) {
+    TimingSlot& t = g_timing_slots[i];
+    if (cudaEventSynchronize(t.e[2]) != cudaSuccess) return VA_ERR_CUDA;
+    float a = 0.f, b = 0.f;
+    if (cudaEventElapsedTime(&a, t.e[0], t.e[1]) != cudaSuccess) return VA_ERR_CUDA;
+    if (cudaEventElapsedTime(&b, t.e[1], t.e[2]) != cudaSuccess) return VA_ERR_CUDA;
+    if (partial_ms) partial_ms[i] = a;
+    if (merge_ms) merge_ms[i] = b;
+  }
+  *num_calls = n;
+  return VA_OK;
+}
+
+va_status verify_attn_chain(const va_problem* p, const va_kv* kv, void* ws, size_t ws_bytes,
+                            float* o, float* lse, uint32_t* status, void* stream) {
+  return run(p, kv, VA_MODE_CHAIN, ws, ws_bytes, o, lse, status, stream);
+}
+
+va_status verify_attn_tree(const va_problem* p, const va_kv* kv, void* ws, size_t ws_bytes,
+                           float* o, float* lse, uint32_t* status, void* stream) {
+  return run(p, kv, VA_MODE_TREE, ws, ws_bytes, o, lse, status, stream);
+}
+
+va_status verify_attn_mixed(const va_problem* p, const va_kv* kv, void* ws, size_t ws_bytes,
+                            float* o, float* lse, uint32_t* status, void* stream) {
+  return run(p, kv, VA_MODE_MIXED, ws, ws_bytes, o, lse, status, stream);
+}
+
+va_status va_debug_row_map(const va_problem* p, int32_t mode, int32_t* row_seq,
+                           uint32_t* anc_mask, uint32_t* status, void* stream) {
+  if (!p || !p->cu_rows || !p->ctx_len) return VA_ERR_INVALID_ARG;
+  if (mode < VA_MODE_CHAIN || mode > VA_MODE_MIXED) return VA_ERR_INVALID_ARG;
+  if (p->num_seqs < 1 || p->max_rows_per_seq < 1 || p->max_rows_per_seq > 32)
+    return VA_ERR_INVALID_ARG;
+  if (mode != VA_MODE_CHAIN && !p->parent) return VA_ERR_INVALID_ARG;
+  if (mode == VA_MODE_MIXED && !p->seq_kind) return VA_ERR_INVALID_ARG;
+  if (p->total_rows == 0) return VA_OK;
+  if (!row_seq || !anc_mask) return VA_ERR_INVALID_ARG;
+  Params q;
+  memset(&q, 0, sizeof(q));
+  q.num_seqs = p->num_seqs;
+  q.total_rows = p->total_rows;
+  q.max_rows = p->max_rows_per_seq;
+  q.mode = mode;
+  q.cu_rows = p->cu_rows;
+  q.ctx_len = p->ctx_len;
+  q.parent = p->parent;
+  q.seq_kind = p->seq_kind;
+  q.status = (unsigned*)status;
+  q.capacity = 1LL << 40;  // spans are not checked here
+  return launch_debug_row_map(q, row_seq, (unsigned*)anc_mask, (cudaStream_t)stream) ==
+                 cudaSuccess
+             ? VA_OK
+             : VA_ERR_CUDA;
+}
+
+va_status va_debug_gather_index(const va_problem* p, const va_kv* kv, int32_t kv_head,
+                                int64_t max_len, int64_t* phys_row, uint32_t* status,
+                                void* stream) {
+  va_status st = check(p, kv, VA_MODE_CHAIN);
+  if (st != VA_OK) return st;
+  if (kv_head < 0 || kv_head >= kv->num_kv_heads || max_len < 1 || !phys_row)
+    return VA_ERR_INVALID_ARG;
+  Plan pl = make_plan(p, kv);
+  Params q = make_params(p, kv, VA_MODE_CHAIN, pl, nullptr, nullptr, nullptr, status);
+  return launch_debug_gather(q, kv_head, (long long)max_len, (long long*)phys_row,
+                             (cudaStream_t)stream) == cudaSuccess
+             ? VA_OK
+             : VA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,171 @@
+// Shared device-side definitions of the verify-attention kernels: launch
+// parameters, the split rule, row masks, the KV gather and storage decoding.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "verify_attn.h"
+
+namespace va {
+
+constexpr int kPage = 16;
+constexpr int kQ8Block = 32;
+constexpr int kQ8BlockBytes = 34;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Everything a partial / merge / debug kernel needs, passed by value.
+struct Params {
+  int num_seqs, H, KVH, G, D;
+  int total_rows, max_rows;
+  int S, P, slots;        // logical splits, sub-chunks per split, S*P
+  int min_sub;            // smallest sub-chunk (tokens) before a split is cut further
+  int mode;               // va_mode
+  int kv_dtype, q_dtype;  // va_dtype
+  float scale_log2;       // softmax scale * log2(e)
+  const void* q;
+  const int* cu_rows;
+  const int* ctx_len;
+  const int* parent;
+  const unsigned char* seq_kind;
+  const void* k;
+  const void* v;
+  int page_size;
+  long long capacity;
+  const int* block_table;
+  int max_blocks;
+  int num_blocks;
+  int row_bytes;          // bytes of one (token, KV head) row
+  float* ws_acc;          // [slots][total_rows][H][D]
+  float* ws_ml;           // [slots][total_rows][H][2]  (m in log2 units, l)
+  float* o;               // [total_rows][H][D]
+  float* lse;             // [total_rows][H]
+  unsigned* status;
+  int rows_per_block;     // query rows (j, g pairs) one partial CTA owns
+  int row_blocks;         // ceil(max_rows * G / rows_per_block)
+};
+
+__device__ __forceinline__ void flag(unsigned* status, unsigned bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// Split rule: chunk = ceil(L/S) rounded up to 16 tokens; split s covers
+// [s*chunk, min((s+1)*chunk, L)).  Sub-chunk p of P covers a 16-aligned
+// slice of that range; the number of live sub-chunks depends only on the
+// chunk's own length.  Nothing here looks at other sequences.
+__device__ __forceinline__ void split_range(int L, int S, int s, int* lo, int* hi) {
+  int per = (L + S - 1) / S;
+  int chunk = (per + kPage - 1) / kPage * kPage;
+  long long a = (long long)s * chunk, b = (long long)(s + 1) * chunk;
+  *lo = (int)(a < L ? a : L);
+  *hi = (int)(b < L ? b : L);
+}
+
+__device__ __forceinline__ void sub_range(int lo, int hi, int P, int min_sub, int p, int* slo,
+                                          int* shi) {
+  int len = hi - lo;
+  int live = (len + min_sub - 1) / min_sub;
+  if (live > P) live = P;
+  if (live < 1) live = 1;
+  if (p >= live) {
+    *slo = *shi = hi;
+    return;
+  }
+  int per = (len + live - 1) / live;
+  int sub = (per + kPage - 1) / kPage * kPage;
+  long long a = lo + (long long)p * sub, b = lo + (long long)(p + 1) * sub;
+  *slo = (int)(a < hi ? a : hi);
+  *shi = (int)(b < hi ? b : hi);
+}
+
+// Kind of sequence s: 0 chain / direct, 1 tree.
+__device__ __forceinline__ int seq_kind_of(const Params& p, int s) {
+  if (p.mode == VA_MODE_CHAIN) return 0;
+  if (p.mode == VA_MODE_TREE) return 1;
+  return p.seq_kind[s] ? 1 : 0;
+}
+
+// Ancestor mask of local row j: bit a set iff draft position a is visible
+// to row j (a == j or a is an ancestor).  The walk strictly decreases, so it
+// ends within j steps; a parent outside [-1, current) flags an error.
+__device__ __forceinline__ unsigned row_mask(int kind, const int* parent_seq, int j,
+                                             bool* bad) {
+  if (kind == 0) return j >= 31 ? 0xFFFFFFFFu : ((1u << (j + 1)) - 1u);
+  unsigned m = 1u << j;
+  int cur = j;
+  int par = parent_seq[j];
+  while (par != -1) {
+    if (par < -1 || par >= cur) {
+      *bad = true;
+      return m;
+    }
+    m |= 1u << par;
+    cur = par;
+    par = parent_seq[cur];
+  }
+  return m;
+}
+
+// Row of token t of (sequence s, KV head kvh), counted in rows of the k/v
+// array; -1 when the block table entry is out of range.
+__device__ __forceinline__ long long kv_row(const Params& p, int s, int kvh, int t) {
+  if (p.page_size == 0) return ((long long)s * p.KVH + kvh) * p.capacity + t;
+  int blk = p.block_table[(long long)s * p.max_blocks + t / kPage];
+  if (blk < 0 || blk >= p.num_blocks) return -1;
+  return ((long long)blk * p.KVH + kvh) * kPage + (t % kPage);
+}
+
+// Validate sequence s: row count and the span against capacity / the block
+// table.  Returns the error bits (0 if fine).
+__device__ __forceinline__ unsigned check_sequence(const Params& p, int s, int* row0, int* n,
+                                                   int* ctx) {
+  int r0 = p.cu_rows[s], r1 = p.cu_rows[s + 1];
+  int c = p.ctx_len[s];
+  *row0 = r0;
+  *n = r1 - r0;
+  *ctx = c;
+  unsigned err = 0;
+  if (r1 < r0 || r1 - r0 > p.max_rows || r0 < 0 || r1 > p.total_rows) err |= VA_DEV_BAD_ROWS;
+  if (c < 0) err |= VA_DEV_CTX_OVERFLOW;
+  if (!err) {
+    long long L = (long long)c + (r1 - r0);
+    if (p.page_size == 0) {
+      if (L > p.capacity) err |= VA_DEV_CTX_OVERFLOW;
+    } else {
+      if ((L + kPage - 1) / kPage > p.max_blocks) err |= VA_DEV_CTX_OVERFLOW;
+    }
+  }
+  return err;
+}
+
+// Storage decoding (exact for bf16 and fp16 scales; Q8 element = d*q in fp32).
+__device__ __forceinline__ float bf16_bits_to_float(unsigned short b) {
+  return __uint_as_float(((unsigned)b) << 16);
+}
+
+__device__ __forceinline__ float load_q(const Params& p, long long idx) {
+  if (p.q_dtype == VA_F32) return reinterpret_cast<const float*>(p.q)[idx];
+  return bf16_bits_to_float(reinterpret_cast<const unsigned short*>(p.q)[idx]);
+}
+
+template <int KVT>
+__device__ __forceinline__ float load_kv(const void* base, long long row, int row_bytes, int d) {
+  const unsigned char* r = reinterpret_cast<const unsigned char*>(base) + row * row_bytes;
+  if (KVT == VA_F32) return reinterpret_cast<const float*>(r)[d];
+  if (KVT == VA_BF16) return bf16_bits_to_float(reinterpret_cast<const unsigned short*>(r)[d]);
+  const unsigned char* blk = r + (d / kQ8Block) * kQ8BlockBytes;
+  unsigned short sb = (unsigned short)(blk[0] | (blk[1] << 8));
+  float sc = __half2float(__ushort_as_half(sb));
+  signed char code = (signed char)blk[2 + (d % kQ8Block)];
+  return sc * (float)code;
+}
+
+// Index of the partial slot for (slot, global row, head).
+__device__ __forceinline__ long long slot_index(const Params& p, int slot, int grow, int h) {
+  return ((long long)slot * p.total_rows + grow) * p.H + h;
+}
+
+}  // namespace va

@@ -1,0 +1,56 @@
+// Debug exports of the row map, ancestor masks and KV gather: they call the
+// same device functions the partial kernels use, so a bit-exact comparison
+// with the oracle checks the kernels' own indexing.
+#include "va_common.cuh"
+
+namespace va {
+
+// One thread per (sequence, local row slot up to max_rows).
+__global__ void debug_row_map_kernel(const Params p, int* row_seq, unsigned* anc) {
+  const int s = blockIdx.x;
+  const int j = threadIdx.x;
+  int row0, n, ctx;
+  unsigned err = check_sequence(p, s, &row0, &n, &ctx);
+  if (err & VA_DEV_BAD_ROWS) {
+    if (j == 0) flag(p.status, err & VA_DEV_BAD_ROWS);
+    return;
+  }
+  if (j >= n) return;
+  bool bad = false;
+  unsigned m = row_mask(seq_kind_of(p, s), p.parent + row0, j, &bad);
+  if (bad) flag(p.status, VA_DEV_BAD_PARENT);
+  row_seq[row0 + j] = s;
+  anc[row0 + j] = m;
+}
+
+// One thread per (sequence, token < max_len).
+__global__ void debug_gather_kernel(const Params p, int kvh, long long max_len, long long* out) {
+  const int s = blockIdx.y;
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= max_len) return;
+  int row0, n, ctx;
+  unsigned err = check_sequence(p, s, &row0, &n, &ctx);
+  long long L = (long long)ctx + n;
+  long long v = -1;
+  if (err) {
+    if (t == 0) flag(p.status, err);
+  } else if (t < L) {
+    v = kv_row(p, s, kvh, (int)t);
+    if (v < 0) flag(p.status, VA_DEV_BAD_BLOCK);
+  }
+  out[(long long)s * max_len + t] = v;
+}
+
+cudaError_t launch_debug_row_map(const Params& p, int* row_seq, unsigned* anc, cudaStream_t st) {
+  debug_row_map_kernel<<<p.num_seqs, 32, 0, st>>>(p, row_seq, anc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_gather(const Params& p, int kvh, long long max_len, long long* out,
+                                cudaStream_t st) {
+  dim3 grid((unsigned)((max_len + 255) / 256), p.num_seqs);
+  debug_gather_kernel<<<grid, 256, 0, st>>>(p, kvh, max_len, out);
+  return cudaGetLastError();
+}
+
+}  // namespace va
