@@ -52,6 +52,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kernel", default="auto", choices=["auto", "cuda-cores"])
+    ap.add_argument("--profile", action="store_true",
+                    help="profiling run for ncu: W + K eager calls of the headline workload "
+                         "(--ctx selects the context), no graphs, no JSON line")
+    ap.add_argument("--ctx", type=int, default=HEADLINE_CTX)
     return ap.parse_args()
 
 
@@ -255,28 +259,38 @@ class Bench:
                 self.call(i)
             self.singles.append(g)
         self.block_calls = calls_per_graph
-        # create the library's timing events eagerly, then capture with them
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for i in range(calls_per_graph):
+                self.call(i)
+        self.block = g
+        # The instrumented copy: the library records per-kernel events inside
+        # the graph (created eagerly first).  An event between the partial
+        # and merge kernels also stops the merge's early (programmatic)
+        # launch, so the plain graph gives the per-call time and this one the
+        # per-kernel durations.
         self.va.timing_enable(True)
         for i in range(calls_per_graph):
             self.call(i)
         torch.cuda.synchronize()
         self.va.timing_enable(True)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=self.stream):
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=self.stream):
             for i in range(calls_per_graph):
                 self.call(i)
         self.va.timing_enable(False)
-        self.block = g
+        self.block_timed = g2
         torch.cuda.synchronize()
 
-    def replay(self, calls):
+    def replay(self, calls, instrumented=False):
         nb, rem = divmod(calls, self.block_calls)
+        blk = self.block_timed if instrumented else self.block
         for _ in range(nb):
-            self.block.replay()
+            blk.replay()
         for i in range(rem):
             self.singles[i % self.copies].replay()
 
-    def timed(self, calls, world):
+    def timed(self, calls, world, instrumented=False):
         import torch
         torch.cuda.synchronize()
         barrier(world)
@@ -285,7 +299,7 @@ class Bench:
         e1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(self.stream):
             e0.record(self.stream)
-            self.replay(calls)
+            self.replay(calls, instrumented)
             e1.record(self.stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -376,6 +390,7 @@ def run_ours(args):
         b.replay(calls_per_graph * 8)
         torch.cuda.synchronize()
     ms = b.timed(args.steps, world)
+    ms_instr = b.timed(args.steps, world, instrumented=True)
     partial_ms, merge_ms = va.timing_read(calls_per_graph)
     t_end = time.time() + 0.5
     while time.time() < t_end:
@@ -404,6 +419,7 @@ def run_ours(args):
         b2.capture(4 * b2.copies)
         n2 = max(4 * b2.copies, min(args.steps, 400))
         ms2 = max_over_ranks(b2.timed(n2, world), world)
+        b2.timed(n2, world, instrumented=True)
         pm, mm = va.timing_read(4 * b2.copies)
         us = ms2 / n2 * 1e3
         contexts[str(ctx)] = {"us_per_call": us, "kv_gbs": c2.kv_bytes / (us * 1e-6) / 1e9,
@@ -432,9 +448,14 @@ def run_ours(args):
                          f"({b.copies * b.kv.k.numel() * 2 / 2 ** 20:.0f} MiB >= 3x L2 "
                          f"{l2 / 2 ** 20:.0f} MiB)",
                    "launch": "CUDA graphs of library calls, "
-                             f"{calls_per_graph} calls per graph",
+                             f"{calls_per_graph} calls per graph; merge launched as a "
+                             "programmatic dependent of the partial kernel",
+                   "kernel_timing": "per-kernel CUDA events recorded by the library inside "
+                                    "an identical graph, timed right after the headline "
+                                    "region over the same number of calls",
                    "plan": b.plan},
         "us_per_call": per_call_ms * 1e3,
+        "us_per_call_instrumented": ms_instr / args.steps * 1e3,
         "hbm_frac_call": value / world / peak,
         "contexts": contexts,
         "roofline": {"kernel": kernel_name, "bound": "hbm", "achieved": achieved, "peak": peak,
@@ -449,8 +470,33 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """Eager calls only, for ncu: the kernels exactly as the bench launches
+    them, without graph capture, timing events or the CPU legs."""
+    import torch
+
+    import speculative_decoding_verify_kv_gb300 as va
+    import synthetic as sy
+    torch.cuda.set_device(0)
+    flags = va.FLAG_CUDA_CORES if args.kernel == "cuda-cores" else 0
+    case = sy.long_q8(ctx=args.ctx, num_splits=SPLITS)
+    l2 = int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2 ** 20))
+    b = Bench(case, flags, l2)
+    for i in range(args.warmup + args.steps):
+        b.call(i)
+    torch.cuda.synchronize()
+    st = int(b.status.item())
+    print(f"profile run: {args.warmup + args.steps} calls, ctx {args.ctx}, status {st:#x}, "
+          f"plan {b.plan}")
+    if st:
+        sys.exit(1)
+
+
 def main():
     args = parse()
+    if args.profile:
+        run_profile(args)
+        return
     if args.impl == "reference":
         run_reference(args)
         return

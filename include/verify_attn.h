@@ -146,6 +146,9 @@ int32_t va_version(void);
 /* Human-readable name of a status code; never NULL. */
 const char *va_status_string(va_status s);
 
+/* Text of the CUDA error behind this thread's last VA_ERR_CUDA; never NULL. */
+const char *va_last_cuda_error(void);
+
 /*
  * Bytes of device workspace a verify call needs for this problem: the fp32
  * split partials (m, l and the unnormalised accumulator per split, row and

@@ -32,7 +32,7 @@ STATUS_NAMES = {0: "VA_OK", 1: "VA_ERR_INVALID_ARG", 2: "VA_ERR_UNSUPPORTED",
 DTYPE_CODES = {"f32": F32, "bf16": BF16, "q8_0": Q8_0}
 MODE_CODES = {"chain": MODE_CHAIN, "tree": MODE_TREE, "mixed": MODE_MIXED}
 
-EXPORTED = ["va_version", "va_status_string", "va_workspace_size", "va_validate",
+EXPORTED = ["va_version", "va_status_string", "va_last_cuda_error", "va_workspace_size", "va_validate",
             "verify_attn_chain", "verify_attn_tree", "verify_attn_mixed",
             "va_debug_row_map", "va_debug_gather_index", "va_plan", "va_timing_enable",
             "va_timing_read"]
@@ -73,6 +73,7 @@ def _load():
     lib.va_version.restype = ctypes.c_int32
     lib.va_status_string.restype = ctypes.c_char_p
     lib.va_status_string.argtypes = [ctypes.c_int]
+    lib.va_last_cuda_error.restype = ctypes.c_char_p
     lib.va_workspace_size.restype = ctypes.c_size_t
     lib.va_workspace_size.argtypes = [P(VaProblem), P(VaKV)]
     lib.va_validate.restype = ctypes.c_int
@@ -106,8 +107,9 @@ LIB_PATH = _build.lib_path()
 class VaError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
+        extra = f": {lib.va_last_cuda_error().decode()}" if code == 5 else ""
         super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} "
-                         f"({lib.va_status_string(code).decode()})")
+                         f"({lib.va_status_string(code).decode()}{extra})")
 
 
 def _ptr(t) -> Optional[int]:

@@ -17,6 +17,15 @@
 namespace va {
 cudaError_t launch_simt_partial(const Params& p, dim3 grid, cudaStream_t st);
 int simt_smem_bytes(int D);
+cudaError_t launch_umma_partial(const Params& p, dim3 grid, cudaStream_t st);
+int umma_smem_bytes(int D, int kv_dtype);
+int umma_threads(int D, int kv_dtype);
+
+static thread_local cudaError_t g_last_cuda = cudaSuccess;
+static va_status note_cuda(cudaError_t e) {
+  g_last_cuda = e;
+  return VA_ERR_CUDA;
+}
 cudaError_t launch_merge(const Params& p, cudaStream_t st);
 cudaError_t launch_debug_row_map(const Params& p, int* row_seq, unsigned* anc, cudaStream_t st);
 cudaError_t launch_debug_gather(const Params& p, int kvh, long long max_len, long long* out,
@@ -24,6 +33,7 @@ cudaError_t launch_debug_gather(const Params& p, int kvh, long long max_len, lon
 
 constexpr int kSimtRowsPerBlock = 16;
 constexpr int kSimtThreadsPerBlock = 128;
+constexpr int kUmmaRowsPerBlock = 128;
 constexpr int kMinSubTokens = 256;
 constexpr int kMaxSubSplits = 16;
 
@@ -94,13 +104,16 @@ struct Plan {
 static Plan make_plan(const va_problem* p, const va_kv* kv) {
   Plan pl;
   const int G = p->num_heads / kv->num_kv_heads;
-  pl.kernel = 0;
-  pl.rows_per_block = kSimtRowsPerBlock;
-  pl.threads = kSimtThreadsPerBlock;
-  pl.smem = simt_smem_bytes(kv->head_dim);
+  // Kernel choice from the cache dtype and the caller's flag only.
+  const bool tensor = kv->dtype != VA_F32 && !(p->flags & VA_FLAG_CUDA_CORES);
+  pl.kernel = tensor ? 1 : 0;
+  pl.rows_per_block = tensor ? kUmmaRowsPerBlock : kSimtRowsPerBlock;
+  pl.threads = tensor ? umma_threads(kv->head_dim, kv->dtype) : kSimtThreadsPerBlock;
+  pl.smem = tensor ? umma_smem_bytes(kv->head_dim, kv->dtype) : simt_smem_bytes(kv->head_dim);
   // Sub-chunks per split from S, the KV head count and the SM count only:
-  // never from the other sequences of the launch.
-  const int target = 2 * sm_count();
+  // never from the other sequences of the launch.  The tensor-core kernel
+  // holds one CTA per SM, the CUDA-core kernel about two.
+  const int target = (tensor ? 1 : 2) * sm_count();
   int P = target / (p->num_splits * kv->num_kv_heads);
   if (P < 1) P = 1;
   if (P > kMaxSubSplits) P = kMaxSubSplits;
@@ -181,6 +194,19 @@ static bool g_timing_on = false;
 static int g_timing_next = 0;
 constexpr int kMaxTimingSlots = 4096;
 
+// Record a timing event; under stream capture as an external event node.
+// Timing is best-effort: a failed record clears its error so it never
+// reaches the launch checks.
+static void timing_record(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t r = cudaStreamIsCapturing(s, &cap);
+  if (r == cudaSuccess && cap == cudaStreamCaptureStatusActive)
+    r = cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    r = cudaEventRecord(e, s);
+  if (r != cudaSuccess) cudaGetLastError();
+}
+
 static TimingSlot* timing_slot() {
   if (!g_timing_on || g_timing_next >= kMaxTimingSlots) return nullptr;
   if (g_timing_next >= (int)g_timing_slots.size()) {
@@ -206,13 +232,16 @@ static va_status run(const va_problem* p, const va_kv* kv, int mode, void* ws, s
   Params q = make_params(p, kv, mode, pl, ws, o, lse, status);
   cudaStream_t cs = (cudaStream_t)stream;
   TimingSlot* ts = timing_slot();
-  if (ts) cudaEventRecord(ts->e[0], cs);
-  cudaError_t e = launch_simt_partial(q, pl.grid, cs);
-  if (e != cudaSuccess) return VA_ERR_CUDA;
-  if (ts) cudaEventRecord(ts->e[1], cs);
+  // External records so that, under stream capture, they become event
+  // nodes of the graph (plain records only order work inside a capture).
+  if (ts) timing_record(ts->e[0], cs);
+  cudaError_t e = pl.kernel == 1 ? launch_umma_partial(q, pl.grid, cs)
+                                 : launch_simt_partial(q, pl.grid, cs);
+  if (e != cudaSuccess) return note_cuda(e);
+  if (ts) timing_record(ts->e[1], cs);
   e = launch_merge(q, cs);
-  if (e != cudaSuccess) return VA_ERR_CUDA;
-  if (ts) cudaEventRecord(ts->e[2], cs);
+  if (e != cudaSuccess) return note_cuda(e);
+  if (ts) timing_record(ts->e[2], cs);
   return VA_OK;
 }
 
@@ -223,6 +252,8 @@ using namespace va;
 extern "C" {
 
 int32_t va_version(void) { return 100; }
+
+const char* va_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda); }
 
 const char* va_status_string(va_status s) {
   switch (s) {
@@ -279,10 +310,11 @@ va_status va_timing_read(int32_t max_calls, float* partial_ms, float* merge_ms,
   int n = g_timing_next < max_calls ? g_timing_next : max_calls;
   for (int i = 0; i < n; ++i) {
     TimingSlot& t = g_timing_slots[i];
-    if (cudaEventSynchronize(t.e[2]) != cudaSuccess) return VA_ERR_CUDA;
+    cudaError_t e = cudaEventSynchronize(t.e[2]);
+    if (e != cudaSuccess) return note_cuda(e);
     float a = 0.f, b = 0.f;
-    if (cudaEventElapsedTime(&a, t.e[0], t.e[1]) != cudaSuccess) return VA_ERR_CUDA;
-    if (cudaEventElapsedTime(&b, t.e[1], t.e[2]) != cudaSuccess) return VA_ERR_CUDA;
+    if ((e = cudaEventElapsedTime(&a, t.e[0], t.e[1])) != cudaSuccess) return note_cuda(e);
+    if ((e = cudaEventElapsedTime(&b, t.e[1], t.e[2])) != cudaSuccess) return note_cuda(e);
     if (partial_ms) partial_ms[i] = a;
     if (merge_ms) merge_ms[i] = b;
   }
@@ -327,10 +359,8 @@ va_status va_debug_row_map(const va_problem* p, int32_t mode, int32_t* row_seq,
   q.seq_kind = p->seq_kind;
   q.status = (unsigned*)status;
   q.capacity = 1LL << 40;  // spans are not checked here
-  return launch_debug_row_map(q, row_seq, (unsigned*)anc_mask, (cudaStream_t)stream) ==
-                 cudaSuccess
-             ? VA_OK
-             : VA_ERR_CUDA;
+  cudaError_t e = launch_debug_row_map(q, row_seq, (unsigned*)anc_mask, (cudaStream_t)stream);
+  return e == cudaSuccess ? VA_OK : note_cuda(e);
 }
 
 va_status va_debug_gather_index(const va_problem* p, const va_kv* kv, int32_t kv_head,
@@ -342,10 +372,9 @@ va_status va_debug_gather_index(const va_problem* p, const va_kv* kv, int32_t kv
     return VA_ERR_INVALID_ARG;
   Plan pl = make_plan(p, kv);
   Params q = make_params(p, kv, VA_MODE_CHAIN, pl, nullptr, nullptr, nullptr, status);
-  return launch_debug_gather(q, kv_head, (long long)max_len, (long long*)phys_row,
-                             (cudaStream_t)stream) == cudaSuccess
-             ? VA_OK
-             : VA_ERR_CUDA;
+  cudaError_t e = launch_debug_gather(q, kv_head, (long long)max_len, (long long*)phys_row,
+                                      (cudaStream_t)stream);
+  return e == cudaSuccess ? VA_OK : note_cuda(e);
 }
 
 }  // extern "C"

@@ -40,6 +40,8 @@ __global__ void __launch_bounds__(kSimtThreads) simt_partial_kernel(const Params
   __shared__ unsigned mask_s[kSimtRows];
   __shared__ int bad_s;
 
+  // The merge kernel may launch now; it waits for this grid to finish.
+  asm volatile("griddepcontrol.launch_dependents;");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rb = blockIdx.x % p.row_blocks;
   const int sp = blockIdx.x / p.row_blocks;
