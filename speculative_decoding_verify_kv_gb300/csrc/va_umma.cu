@@ -41,6 +41,7 @@ namespace va {
 using namespace sm100;
 
 constexpr int kNT = 64;      // tokens per tile
+constexpr int kPrefetch = 4; // L2 prefetch distance in tiles (Q8 raw stream)
 constexpr int kM = 128;      // MMA rows (query rows per CTA)
 constexpr uint64_t kWaitNs = 2000000000ull;
 
@@ -52,18 +53,22 @@ struct UCfg {
   static constexpr int DBLK = D / 64;                    // 64-element column blocks
   static constexpr int TILE = kNT * D * 2;               // one 16-bit tile in smem
   static constexpr int RAW_HALF = kNT * RB;              // raw K (or V) bytes of a tile
-  static constexpr int NRH = (D == 256) ? 4 : (D == 128 ? 8 : 16);  // Q8 raw half-slots
+  static constexpr int NB16 = 3;                         // Q8 tile buffers per tensor
   static constexpr int NST = (D == 256) ? 3 : (D == 128 ? 6 : 8);  // bf16 K+V stages
   static constexpr int COL_O = 0;
   static constexpr int COL_S0 = D;
   static constexpr int COL_Q = D + 2 * kNT;
   static constexpr int TMEM_COLS = (COL_Q + D / 2 <= 256) ? 256 : 512;
   static constexpr int DQ_WARPS = kQ8 ? 8 : 1;
-  static constexpr int THREADS = (10 + DQ_WARPS) * 32;
+  // Q8: warps 10..19 minus 13 and 17, so that the MMA issuer's sub-partition
+  // (warp index = 1 mod 4) carries no dequantisation traffic.
+  static constexpr int THREADS = (kQ8 ? 20 : 11) * 32;
   static constexpr int MAXREG = (65536 / THREADS) / 8 * 8 > 255 ? 255 : (65536 / THREADS) / 8 * 8;
-  static constexpr int SMEM_Q8 = 4 * TILE + NRH * RAW_HALF;
+  static constexpr int SMEM_Q8 = 2 * NB16 * TILE;
   static constexpr int SMEM_BF16 = NST * 2 * TILE;
-  static constexpr int SMEM = (kQ8 ? SMEM_Q8 : SMEM_BF16) + 1024 + 64;
+  static constexpr int SMEM_EPI = kM * (D * 4 + 16);  // O staging at the end
+  static constexpr int SMEM_MAIN = kQ8 ? SMEM_Q8 : SMEM_BF16;
+  static constexpr int SMEM = (SMEM_MAIN > SMEM_EPI ? SMEM_MAIN : SMEM_EPI) + 1024 + 64;
 };
 
 // Barrier slots in static shared memory.
@@ -74,14 +79,17 @@ enum {
   B_QREADY = 5,
   B_DRAIN = 6,
   B_OFINAL = 7,   // the last P.V has completed
-  B_KREADY = 8,   // Q8: [2]
-  B_KEMPTY = 10,  // Q8: [2]
-  B_VREADY = 12,  // Q8: [2]; bf16: [NST]
-  B_VEMPTY = 20,  // Q8: [2]
-  B_RFULL = 22,   // Q8 raw half-slots: [NRH]; bf16 K full: [NST]
-  B_REMPTY = 38,  // Q8 raw half-slots: [NRH]; bf16 stage empty: [NST]
-  B_VFULL = 54,   // bf16 V full: [NST]
-  B_COUNT = 62
+  // Q8 tile buffers, [tensor 0 = K / 1 = V][3]: raw bytes landed, fp16 ready,
+  // buffer free again.
+  B_QFULL = 8,    // [2][3]
+  B_QREADY8 = 14, // [2][3]
+  B_QEMPTY = 20,  // [2][3]
+  // bf16 stages [NST]: K landed, V landed, V fixed up, stage free.
+  B_RFULL = 26,
+  B_VFULL = 34,
+  B_VREADY = 42,
+  B_REMPTY = 50,
+  B_COUNT = 58
 };
 
 // Byte offset of element (row, col) inside one 128-byte-swizzled column
@@ -90,74 +98,98 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int chunk16) {
   return (uint32_t)(row * 128 + ((chunk16 ^ (row & 7)) << 4));
 }
 
-// Dequantise a tile of Q8_0 rows (raw, rows RB bytes apart) into the fp16
-// MMA layout at dst; tokens >= valid become zeros.  128 threads; each takes
-// its 34-byte blocks two at a time with both blocks' shared-memory loads in
-// flight.  Eight consecutive threads take eight consecutive tokens of one
-// block, so their 16-byte stores land in distinct bank groups.
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Dequantise, in place, the raw Q8_0 rows (RB bytes apart) at the start of
+// a tile buffer into the fp16 MMA layout of the same buffer; tokens >= valid
+// become zeros.  128 threads (named barrier `barid`): thread -> (token
+// t = tid % 64, half-row hf = tid / 64).  Phase A reads every raw byte the
+// thread needs into registers, the barrier waits for all readers, phase B
+// writes the fp16 rows (eight consecutive threads take eight consecutive
+// tokens of one block, so their 16-byte stores hit distinct bank groups).
 template <int D>
-__device__ __forceinline__ void dequant_tile(const unsigned char* raw, unsigned char* dst,
-                                             int valid, int tid) {
-  constexpr int NB = D / 32;
-  constexpr int RB = NB * 34;
-  constexpr int ITEMS = kNT * NB;
-  constexpr int NTHR = 128;
-#pragma unroll 1
-  for (int u0 = tid; u0 < ITEMS; u0 += 2 * NTHR) {
-    uint32_t wd[2][9];
-    int tt[2], bq[2];
-    bool live[2];
+__device__ __forceinline__ void dequant_inplace(unsigned char* buf, int valid, int tid, int barid,
+                                                bool work) {
+  constexpr int NB = D / 32;      // blocks per row
+  constexpr int RB = NB * 34;     // bytes per row
+  constexpr int HB = RB / 2;      // bytes per half-row
+  constexpr int NBH = NB / 2;     // blocks per half-row
+  constexpr int NW = (HB + 2 + 3) / 4 + 1;
+  const int t = tid & 63, hf = tid >> 6;
+  const int start = t * RB + hf * HB;
+  const int sh = start & 3;       // 0 or 2
+  uint32_t w[NW];
+  const bool live = work && t < valid;
+  if (live) {
+    if (D == 256 && hf == 0) {
+      // 16-byte aligned: 9 x 16-byte loads (the last 8 bytes belong to hf 1).
+      const uint4* q = reinterpret_cast<const uint4*>(buf + start);
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int u = u0 + k * NTHR;
-      tt[k] = (u & 7) + 8 * (u / (8 * NB));
-      bq[k] = (u >> 3) % NB;
-      live[k] = u < ITEMS;
-      if (live[k] && tt[k] < valid) {
-        const int off = tt[k] * RB + bq[k] * 34;
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(raw + (off & ~3));
-#pragma unroll
-        for (int q = 0; q < 9; ++q) wd[k][q] = w[q];
+      for (int k = 0; k < 9; ++k) {
+        const uint4 v = q[k];
+        w[4 * k] = v.x;
+        w[4 * k + 1] = v.y;
+        w[4 * k + 2] = v.z;
+        w[4 * k + 3] = v.w;
       }
+    } else if (D == 256) {
+      // 8-byte aligned half-row.
+      const uint2* q = reinterpret_cast<const uint2*>(buf + start);
+#pragma unroll
+      for (int k = 0; k < 17; ++k) {
+        const uint2 v = q[k];
+        w[2 * k] = v.x;
+        w[2 * k + 1] = v.y;
+      }
+    } else {
+      const uint32_t* q = reinterpret_cast<const uint32_t*>(buf + (start - sh));
+#pragma unroll
+      for (int k = 0; k < NW; ++k) w[k] = q[k];
     }
+  }
+  named_barrier_sync(barid, 128);
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      if (!live[k]) continue;
-      const int t = tt[k], b = bq[k];
-      unsigned char* drow = dst + (b >> 1) * (kNT * 128);
-      const int c0 = (b & 1) * 4;
-      uint4 out[4];
-      if (t < valid) {
-        uint32_t sbits, code[8];
-        if (b & 1) {  // block starts 2 bytes past a word boundary
-          sbits = wd[k][0] >> 16;
+  for (int jb = 0; jb < NBH; ++jb) {
+    const int b = hf * NBH + jb;                 // block index in the row
+    unsigned char* drow = buf + (b >> 1) * (kNT * 128);
+    const int c0 = (b & 1) * 4;
+    uint4 out[4];
+    if (live) {
+      const int o = sh + 34 * jb;                // block offset in the thread's words
+      const int wo = o >> 2;
+      uint32_t sbits, code[8];
+      if (o & 2) {
+        sbits = w[wo] >> 16;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) code[q] = wd[k][q + 1];
-        } else {
-          sbits = wd[k][0] & 0xFFFFu;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) code[q] = __funnelshift_r(wd[k][q], wd[k][q + 1], 16);
-        }
-        const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)sbits));
-        const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
-        uint32_t hv[16];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint32_t x = code[q] ^ 0x80808080u;  // bytes q + 128
-          uint32_t lo = __byte_perm(x, 0x64646464u, 0x4140);
-          uint32_t hi = __byte_perm(x, 0x64646464u, 0x4342);
-          __half2 a = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&lo), bias), d2);
-          __half2 c = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&hi), bias), d2);
-          hv[2 * q] = *reinterpret_cast<uint32_t*>(&a);
-          hv[2 * q + 1] = *reinterpret_cast<uint32_t*>(&c);
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          out[c] = make_uint4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
+        for (int q = 0; q < 8; ++q) code[q] = w[wo + 1 + q];
       } else {
+        sbits = w[wo] & 0xFFFFu;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) out[c] = make_uint4(0u, 0u, 0u, 0u);
+        for (int q = 0; q < 8; ++q) code[q] = __funnelshift_r(w[wo + q], w[wo + q + 1], 16);
       }
+      const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)sbits));
+      const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
+      uint32_t hv[16];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t x = code[q] ^ 0x80808080u;  // bytes q + 128
+        uint32_t lo = __byte_perm(x, 0x64646464u, 0x4140);
+        uint32_t hi = __byte_perm(x, 0x64646464u, 0x4342);
+        __half2 a = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&lo), bias), d2);
+        __half2 c = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&hi), bias), d2);
+        hv[2 * q] = *reinterpret_cast<uint32_t*>(&a);
+        hv[2 * q + 1] = *reinterpret_cast<uint32_t*>(&c);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        out[c] = make_uint4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) out[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (work) {
 #pragma unroll
       for (int c = 0; c < 4; ++c)
         *reinterpret_cast<uint4*>(drow + sw128_off(t, c0 + c)) = out[c];
@@ -169,10 +201,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-__device__ __forceinline__ void named_barrier_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Pack two probabilities for the P.V MMA: fp16 pair (Q8 path), or bf16
@@ -276,6 +304,52 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
+  // Shared-memory regions.
+  //   Q8: tile buffers K0 V0 K1 V1 K2 V2 (raw Q8 rows land at the start of a
+  //       buffer and are dequantised in place).
+  //   bf16: stages of (K tile, V tile).
+  auto q8buf = [&](int kv, int j) { return sm + (2 * j + kv) * C::TILE; };
+  auto kst = [&](int st) { return sm + st * 2 * C::TILE; };            // bf16 K stage
+  auto vst = [&](int st) { return sm + st * 2 * C::TILE + C::TILE; };  // bf16 V stage
+  // L2 prefetch of the raw Q8 rows of tensor kv (0 = K, 1 = V), tile i.
+  auto prefetch_q8 = [&](int i, int kv) {
+    const unsigned char* src = (const unsigned char*)(kv ? p.v : p.k);
+    const int tp = slo + i * kNT;
+    const int np = min(tp + kNT, (shi + kPage - 1) / kPage * kPage) - tp;
+    if (p.page_size == 0) {
+      const long long rowp = ((long long)s * p.KVH + kvh) * p.capacity + tp;
+      bulk_prefetch_l2(src + rowp * C::RB, (uint32_t)(np * C::RB));
+    } else {
+      for (int pg = 0; pg < np / kPage; ++pg) {
+        const int blk = p.block_table[(long long)s * p.max_blocks + tp / kPage + pg];
+        bulk_prefetch_l2(src + ((long long)blk * p.KVH + kvh) * kPage * C::RB, kPage * C::RB);
+      }
+    }
+  };
+  // Copy the raw Q8 rows of tensor kv, tile i, into buffer i % 3 (whose
+  // previous tile must be consumed), and pull tile i + kPrefetch into L2.
+  auto issue_q8 = [&](int i, int kv) {
+    const int jb = i % C::NB16;
+    const uint64_t pol = policy_evict_first();
+    const int t0 = slo + i * kNT;
+    const int nload = min(t0 + kNT, (shi + kPage - 1) / kPage * kPage) - t0;  // multiple of 16
+    const unsigned char* src = (const unsigned char*)(kv ? p.v : p.k);
+    unsigned char* dst = q8buf(kv, jb);
+    const uint32_t fb = bar(B_QFULL + 3 * kv + jb);
+    if (i + kPrefetch < ntiles) prefetch_q8(i + kPrefetch, kv);
+    mbar_arrive_expect_tx(fb, (uint32_t)(nload * C::RB));
+    if (p.page_size == 0) {
+      const long long rowi = ((long long)s * p.KVH + kvh) * p.capacity + t0;
+      bulk_g2s(smem_u32(dst), src + rowi * C::RB, (uint32_t)(nload * C::RB), fb, pol);
+    } else {
+      for (int pg = 0; pg < nload / kPage; ++pg) {
+        const int blk = p.block_table[(long long)s * p.max_blocks + t0 / kPage + pg];
+        const long long rowi = ((long long)blk * p.KVH + kvh) * kPage;
+        bulk_g2s(smem_u32(dst + pg * kPage * C::RB), src + rowi * C::RB, kPage * C::RB, fb, pol);
+      }
+    }
+  };
+
   if (tid == 0) {
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_SFULL + 1), 1);
@@ -286,15 +360,10 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_OFINAL), 1);
     if (Q8) {
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(bar(B_KREADY + i), C::DQ_WARPS / 2);
-        mbar_init(bar(B_KEMPTY + i), 1);
-        mbar_init(bar(B_VREADY + i), C::DQ_WARPS / 2);
-        mbar_init(bar(B_VEMPTY + i), 1);
-      }
-      for (int i = 0; i < C::NRH; ++i) {
-        mbar_init(bar(B_RFULL + i), 1);
-        mbar_init(bar(B_REMPTY + i), C::DQ_WARPS / 2);
+      for (int i = 0; i < 6; ++i) {
+        mbar_init(bar(B_QFULL + i), 1);
+        mbar_init(bar(B_QREADY8 + i), C::DQ_WARPS / 2);
+        mbar_init(bar(B_QEMPTY + i), 1);
       }
     } else {
       for (int i = 0; i < C::NST; ++i) {
@@ -305,6 +374,16 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       }
     }
     fence_barrier_init();
+    if (Q8) {
+      // Tile 0 goes to buffers K0/V0, which the Q staging does not use:
+      // start the HBM reads before the rest of the prologue.
+      issue_q8(0, 0);
+      issue_q8(0, 1);
+      for (int i = 1; i < min(kPrefetch, ntiles); ++i) {
+        prefetch_q8(i, 0);
+        prefetch_q8(i, 1);
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_base_s), C::TMEM_COLS);
@@ -320,9 +399,10 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     flag(p.status, VA_DEV_TIMEOUT);
   };
 
-  // Q8: warps 2.. stage this CTA's Q rows in shared memory (the fp16 tile
-  // buffers, unused until the first dequant) with every load in flight;
-  // the softmax warps convert them into TMEM, then release the area.
+
+  // Q8: warps 2.. stage this CTA's Q rows in shared memory (tile buffers
+  // K1 onwards) with every load in flight; the softmax warps convert them
+  // into TMEM, and the producer loads tile 1 there only after Q is ready.
   constexpr int kQRow = D * 2 + 16;
   if (Q8 && warp >= 2) {
     constexpr int CPR = D / 8;  // 16-byte chunks per row
@@ -344,52 +424,33 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
 #pragma unroll
     for (int k = 0; k < ITER; ++k) {
       const int c = t + k * NTHR;
-      if (c < total) *reinterpret_cast<uint4*>(sm + (c / CPR) * kQRow + (c % CPR) * 16) = v[k];
+      if (c < total)
+        *reinterpret_cast<uint4*>(sm + 2 * C::TILE + (c / CPR) * kQRow + (c % CPR) * 16) = v[k];
     }
     named_barrier_sync(2, NTHR);
-    if (warp >= 10) named_barrier_sync(2, NTHR);  // dequant warps wait for the release
   }
-
-  // Shared-memory regions.
-  unsigned char* k16 = sm;                      // Q8: 2 dequantised K tiles
-  unsigned char* v16 = sm + 2 * C::TILE;        // Q8: 2 dequantised V tiles
-  unsigned char* raw = sm + 4 * C::TILE;        // Q8: raw stages
-  auto kst = [&](int st) { return sm + st * 2 * C::TILE; };            // bf16 K stage
-  auto vst = [&](int st) { return sm + st * 2 * C::TILE + C::TILE; };  // bf16 V stage
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int issued = 0;
+      int issued = Q8 ? 1 : 0;
       if (Q8) {
-        // Raw K_i and V_i go to their own half-slots (K, V, K, V, ...), each
-        // freed as soon as its own dequantisation is done.
-        for (int hh = 0; hh < 2 * ntiles; ++hh) {
-          const int i = hh >> 1, slot = hh % C::NRH;
-          if (!mbar_wait(bar(B_REMPTY + slot), ((hh / C::NRH) & 1) ^ 1, abort_p, kWaitNs)) {
+        // Buffers K1.. hold the Q staging until the softmax warps have put
+        // Q into TMEM.
+        if (ntiles > 1 && !mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs)) fail();
+        for (int i = 1; i < ntiles && !*abort_p; ++i) {
+          const int jb = i % C::NB16;
+          const uint32_t par = ((i / C::NB16) & 1) ^ 1;
+          bool ok = mbar_wait(bar(B_QEMPTY + jb), par, abort_p, kWaitNs);
+          if (ok) issue_q8(i, 0);
+          ok = ok && mbar_wait(bar(B_QEMPTY + 3 + jb), par, abort_p, kWaitNs);
+          if (ok) issue_q8(i, 1);
+          if (!ok) {
             fail();
             break;
           }
-          const int t0 = slo + i * kNT;
-          const int end16 = min(t0 + kNT, (shi + kPage - 1) / kPage * kPage);
-          const int nload = end16 - t0;  // multiple of 16
-          const unsigned char* src = (const unsigned char*)((hh & 1) ? p.v : p.k);
-          unsigned char* dst = raw + slot * C::RAW_HALF;
-          mbar_arrive_expect_tx(bar(B_RFULL + slot), (uint32_t)(nload * C::RB));
-          if (p.page_size == 0) {
-            const long long rowi = ((long long)s * p.KVH + kvh) * p.capacity + t0;
-            bulk_g2s(smem_u32(dst), src + rowi * C::RB, (uint32_t)(nload * C::RB),
-                     bar(B_RFULL + slot), pol);
-          } else {
-            for (int pg = 0; pg < nload / kPage; ++pg) {
-              const int blk = p.block_table[(long long)s * p.max_blocks + t0 / kPage + pg];
-              const long long rowi = ((long long)blk * p.KVH + kvh) * kPage;
-              bulk_g2s(smem_u32(dst + pg * kPage * C::RB), src + rowi * C::RB, kPage * C::RB,
-                       bar(B_RFULL + slot), pol);
-            }
-          }
-          issued = hh + 1;
+          issued = i + 1;
         }
       } else {
         for (int i = 0; i < ntiles; ++i) {
@@ -433,11 +494,12 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       if (*abort_p) {
         int dummy = 0;
         volatile int* never = &dummy;
-        const int nslot = Q8 ? C::NRH : C::NST;
+        const int nslot = Q8 ? C::NB16 : C::NST;
         for (int i = max(0, issued - nslot); i < issued; ++i) {
           const int st = i % nslot;
-          mbar_wait(bar(B_RFULL + st), (i / nslot) & 1, never, kWaitNs);
-          if (!Q8) mbar_wait(bar(B_VFULL + st), (i / nslot) & 1, never, kWaitNs);
+          const uint32_t par = (i / nslot) & 1;
+          mbar_wait(bar((Q8 ? B_QFULL : B_RFULL) + st), par, never, kWaitNs);
+          mbar_wait(bar((Q8 ? B_QFULL + 3 : B_VFULL) + st), par, never, kWaitNs);
         }
       }
     }
@@ -453,8 +515,9 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
         if (!mbar_wait(bar(B_PFULL + bt), (t >> 1) & 1, abort_p, kWaitNs)) return false;
         uint32_t vaddr;
         if (Q8) {
-          if (!mbar_wait(bar(B_VREADY + bt), (t >> 1) & 1, abort_p, kWaitNs)) return false;
-          vaddr = smem_u32(v16 + bt * C::TILE);
+          const int jb = t % C::NB16;
+          if (!mbar_wait(bar(B_QREADY8 + 3 + jb), (t / C::NB16) & 1, abort_p, kWaitNs)) return false;
+          vaddr = smem_u32(q8buf(1, jb));
         } else {
           const int st = t % C::NST;
           if (!mbar_wait(bar(B_VREADY + st), (t / C::NST) & 1, abort_p, kWaitNs)) return false;
@@ -473,7 +536,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
         }
         any = true;
         mma_commit(bar(B_PVDONE));
-        if (Q8) mma_commit(bar(B_VEMPTY + bt));
+        if (Q8) mma_commit(bar(B_QEMPTY + 3 + t % C::NB16));
         else mma_commit(bar(B_REMPTY + t % C::NST));
         return true;
       };
@@ -483,8 +546,9 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
           const int b = i & 1;
           uint32_t kaddr;
           if (Q8) {
-            ok = mbar_wait(bar(B_KREADY + b), (i >> 1) & 1, abort_p, kWaitNs);
-            kaddr = smem_u32(k16 + b * C::TILE);
+            const int jb = i % C::NB16;
+            ok = mbar_wait(bar(B_QREADY8 + jb), (i / C::NB16) & 1, abort_p, kWaitNs);
+            kaddr = smem_u32(q8buf(0, jb));
           } else {
             const int st = i % C::NST;
             ok = mbar_wait(bar(B_RFULL + st), (i / C::NST) & 1, abort_p, kWaitNs);
@@ -501,7 +565,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
           }
           any = true;
           mma_commit(bar(B_SFULL + b));
-          if (Q8) mma_commit(bar(B_KEMPTY + b));
+          if (Q8) mma_commit(bar(B_QEMPTY + i % C::NB16));
           if (i >= 1) ok = issue_pv(i - 1);
         }
         if (ok) ok = issue_pv(ntiles - 1);
@@ -536,7 +600,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       // Q8: from the shared staging copy (rows padded so the lanes of a warp
       // hit distinct bank groups); bf16: straight from global memory.
       const uint4* qsrc =
-          Q8 ? reinterpret_cast<const uint4*>(sm + r * kQRow + half * D)
+          Q8 ? reinterpret_cast<const uint4*>(sm + 2 * C::TILE + r * kQRow + half * D)
              : reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(p.q) +
                                               ((long long)grow * p.H + h) * D + half * (D / 2));
       float qscale = 1.f;
@@ -589,7 +653,6 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_QREADY));
-      if (Q8) named_barrier_sync(2, C::THREADS - 64);  // staging area free again
     }
 
     float m_use = -INFINITY, l_run = 0.f;
@@ -697,8 +760,11 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       p.ws_ml[2 * si] = bad ? NAN : m_use;
       p.ws_ml[2 * si + 1] = bad ? NAN : l_run + red_l[r];
     }
+    // O rows go through shared memory (the tile buffers are idle now; rows
+    // padded by 16 bytes so a warp's stores hit distinct bank groups) and
+    // leave as one 16-byte-aligned bulk copy per row.
+    constexpr int kORow = D * 4 + 16;
     if (!bad && warp_live) {
-      float* dst = p.ws_acc + si * D;
 #pragma unroll 1
       for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 16) {
         uint32_t o[16];
@@ -707,42 +773,52 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
         if (rvalid) {
 #pragma unroll
           for (int c = 0; c < 16; c += 4)
-            *reinterpret_cast<float4*>(dst + c0 + c) =
-                make_float4(__uint_as_float(o[c]), __uint_as_float(o[c + 1]),
-                            __uint_as_float(o[c + 2]), __uint_as_float(o[c + 3]));
+            *reinterpret_cast<uint4*>(sm + r * kORow + (c0 + c) * 4) =
+                make_uint4(o[c], o[c + 1], o[c + 2], o[c + 3]);
         }
       }
     }
+    fence_proxy_async_smem();
+    named_barrier_sync(1, 256);
+    if (!bad && lane == 0) {
+      // Warp w stores rows w - 2, w + 6, ... (eight warps share the rows).
+      const int nrows_blk = min(kM, R - rb * kM);
+      for (int rr = warp - 2; rr < nrows_blk; rr += 8) {
+        const int rs2 = rb * kM + rr;
+        const long long si2 = slot_index(p, slot, row0 + rs2 / G, kvh * G + rs2 % G);
+        bulk_s2g(p.ws_acc + si2 * D, smem_u32(sm + rr * kORow), D * 4);
+      }
+      bulk_commit();
+      bulk_wait_all();
+    }
   } else {
     // ------------------------------------------------------------ dequant / fix-up
-    if (Q8) {
-      // Warps 10..13 dequantise K tiles, 14..17 V tiles, each group at its
-      // own pace.
-      const int grp = (warp - 10) >> 2;  // 0 = K, 1 = V
-      const int gtid = ((warp - 10) & 3) * 32 + lane;
-      unsigned char* out16 = grp ? v16 : k16;
-      const int b_ready = grp ? B_VREADY : B_KREADY;
-      const int b_empty = grp ? B_VEMPTY : B_KEMPTY;
+    if (Q8 && (warp & 3) != 1) {
+      // Warps 10, 11, 12, 14 dequantise K tiles, 15, 16, 18, 19 V tiles, each
+      // group at its own pace, in place in the tile buffers (13 and 17 idle).
+      const int wq = warp - 10;
+      const int dq = wq - (wq > 3) - (wq > 7);  // 0..7 over warps 10,11,12,14,15,16,18,19
+      const int grp = dq >> 2;                  // 0 = K, 1 = V
+      const int gtid = (dq & 3) * 32 + lane;
+      // A failed wait does not leave the loop: each iteration has one named
+      // barrier shared by the group's four warps, so a failing warp keeps
+      // arriving there (skipping the work) until the loop ends.
+      bool ok = true;
       for (int i = 0; i < ntiles; ++i) {
-        const int hh = 2 * i + grp, slot = hh % C::NRH, buf = i & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_RFULL + slot), (hh / C::NRH) & 1, abort_p, kWaitNs))) {
+        const int jb = i % C::NB16;
+        if (ok && !__all_sync(0xffffffffu, mbar_wait(bar(B_QFULL + 3 * grp + jb),
+                                                     (i / C::NB16) & 1, abort_p, kWaitNs))) {
+          ok = false;
           if (lane == 0) fail();
-          break;
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(b_empty + buf), ((i >> 1) & 1) ^ 1, abort_p, kWaitNs))) {
-          if (lane == 0) fail();
-          break;
-        }
-        const int valid = shi - (slo + i * kNT);
-        dequant_tile<D>(raw + slot * C::RAW_HALF, out16 + buf * C::TILE, valid, gtid);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar(b_ready + buf));
-          mbar_arrive(bar(B_REMPTY + slot));
+        dequant_inplace<D>(q8buf(grp, jb), shi - (slo + i * kNT), gtid, 3 + grp, ok);
+        if (ok) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_QREADY8 + 3 * grp + jb));
         }
       }
-    } else if (warp == 10) {
+    } else if (!Q8 && warp == 10) {
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % C::NST;
         if (!__all_sync(0xffffffffu, mbar_wait(bar(B_VFULL + st), (i / C::NST) & 1, abort_p, kWaitNs))) {
