@@ -228,6 +228,44 @@ va_status va_timing_enable(int32_t on);
 va_status va_timing_read(int32_t max_calls, float *partial_ms, float *merge_ms,
                          int32_t *num_calls);
 
+/*
+ * Verify attention without a caller workspace and without any allocation
+ * on the call path.  The pages have no counterpart: their split-KV route
+ * takes a caller-owned workspace (hipfire PR #817 "Maintainer-review
+ * follow-up"), which verify_attn_chain/tree/mixed keep.
+ *
+ * For callers that cannot hand the library device memory per call: code
+ * that owns no allocator (a plain C host program, a runtime whose device
+ * memory budget is fixed up front), or a serving loop that must not call
+ * into an allocator between steps.  The split partials go to scratch that
+ * belongs to the library: a fixed array of VA_STATIC_WORKSPACE_BYTES in the
+ * library's device image, reserved by the CUDA runtime when the library's
+ * module is loaded on a device (one array per device).
+ *
+ * mode: VA_MODE_CHAIN, VA_MODE_TREE or VA_MODE_MIXED (same meaning as the
+ * three entry points above).  p, kv, o, lse, status, stream: as for
+ * verify_attn_chain.  Nothing needs initialising: the scratch holds no
+ * state between calls and need not start at zero.
+ *
+ * Limits and errors:
+ *   - Problems whose va_workspace_size() exceeds VA_STATIC_WORKSPACE_BYTES
+ *     (16 MiB: e.g. 32 split slots x 16 rows x 24 heads at D=256 fit,
+ *     32 slots x 50 rows x 24 heads do not) return
+ *     VA_ERR_WORKSPACE_TOO_SMALL before any launch; use the entry points
+ *     with a caller workspace for those.
+ *   - The first call on each device looks the scratch address up with
+ *     cudaGetSymbolAddress (VA_ERR_CUDA if that fails); make that first
+ *     call, on every device it will be used on, outside any stream capture.
+ *   - The scratch is shared by every call on a device: calls on one stream
+ *     are ordered and safe, calls that can overlap in time (different
+ *     streams without ordering between them, several host threads) race on
+ *     it and must not be issued.
+ */
+#define VA_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)
+
+va_status verify_attn_noalloc(const va_problem *p, const va_kv *kv, int32_t mode, float *o,
+                              float *lse, uint32_t *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -35,7 +35,7 @@ MODE_CODES = {"chain": MODE_CHAIN, "tree": MODE_TREE, "mixed": MODE_MIXED}
 EXPORTED = ["va_version", "va_status_string", "va_last_cuda_error", "va_workspace_size", "va_validate",
             "verify_attn_chain", "verify_attn_tree", "verify_attn_mixed",
             "va_debug_row_map", "va_debug_gather_index", "va_plan", "va_timing_enable",
-            "va_timing_read"]
+            "va_timing_read", "verify_attn_noalloc"]
 
 
 class VaKV(ctypes.Structure):
@@ -94,6 +94,9 @@ def _load():
     lib.va_plan.argtypes = [P(VaProblem), P(VaKV), ctypes.c_int32, P(VaPlanInfo)]
     lib.va_timing_enable.restype = ctypes.c_int
     lib.va_timing_enable.argtypes = [ctypes.c_int32]
+    lib.verify_attn_noalloc.restype = ctypes.c_int
+    lib.verify_attn_noalloc.argtypes = [P(VaProblem), P(VaKV), ctypes.c_int32, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     lib.va_timing_read.restype = ctypes.c_int
     lib.va_timing_read.argtypes = [ctypes.c_int32, P(ctypes.c_float), P(ctypes.c_float),
                                    P(ctypes.c_int32)]
@@ -228,6 +231,25 @@ def verify_attn_mixed(p: Problem, kv: KV, **kw):
 
 def verify_attn(p: Problem, kv: KV, mode: int, **kw):
     return _call(("verify_attn_chain", "verify_attn_tree", "verify_attn_mixed")[mode], p, kv, **kw)
+
+
+# Bytes of library-held scratch behind verify_attn_noalloc (one array per
+# device, part of the library's device image).
+STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
+
+
+def verify_attn_noalloc(p: Problem, kv: KV, mode: int, o, lse, status=None, stream=None):
+    """Verify call that uses the library's own scratch: no workspace
+    argument and no allocation on the call path (``o`` and ``lse`` are the
+    caller's preallocated outputs).  Raises VaError(VA_ERR_WORKSPACE_TOO_SMALL)
+    for problems that need more than STATIC_WORKSPACE_BYTES of partials.
+    Calls that may overlap in time on one device share the scratch and must
+    not be issued; make the first call per device outside stream capture."""
+    st = lib.verify_attn_noalloc(ctypes.byref(p.c()), ctypes.byref(kv.c()), mode, _ptr(o),
+                                 _ptr(lse), _ptr(status), _stream_handle(stream))
+    if st:
+        raise VaError(st, "verify_attn_noalloc")
+    return o, lse
 
 
 def debug_row_map(p: Problem, mode: int, status=None, stream=None):

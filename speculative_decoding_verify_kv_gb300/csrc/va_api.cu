@@ -10,6 +10,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <vector>
 
 #include "va_common.cuh"
@@ -375,6 +376,71 @@ va_status va_debug_gather_index(const va_problem* p, const va_kv* kv, int32_t kv
   cudaError_t e = launch_debug_gather(q, kv_head, (long long)max_len, (long long*)phys_row,
                                       (cudaStream_t)stream);
   return e == cudaSuccess ? VA_OK : note_cuda(e);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Verify call with library-held scratch (no allocation on the call path).
+//
+// The split partials go to a file-scope device array that is part of this
+// module's device image: the CUDA runtime reserves it when the module is
+// loaded on a device, and this library never allocates or frees it.  Its
+// address on the current device is looked up once per device with
+// cudaGetSymbolAddress and cached.  The partial kernel writes every (m, l)
+// entry of every slot it owns before the merge kernel reads it, and the
+// merge skips slots with l = 0 without reading their accumulators, so no
+// part of the array has to start at zero.  One array per device serves
+// every call: calls on the same stream are ordered, calls that may
+// overlap in time (other streams, other host threads) race on it.
+
+namespace va {
+
+static __device__ __align__(256) unsigned char g_static_ws[VA_STATIC_WORKSPACE_BYTES];
+
+constexpr int kMaxStaticDevices = 64;
+static std::atomic<void*> g_static_ws_ptr[kMaxStaticDevices];
+
+static cudaError_t static_workspace(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxStaticDevices) return cudaErrorInvalidDevice;
+  void* ptr = g_static_ws_ptr[dev].load(std::memory_order_acquire);
+  if (!ptr) {
+    e = cudaGetSymbolAddress(&ptr, g_static_ws);
+    if (e != cudaSuccess) return e;
+    if (!ptr) return cudaErrorInvalidSymbol;
+    g_static_ws_ptr[dev].store(ptr, std::memory_order_release);
+  }
+  *out = ptr;
+  return cudaSuccess;
+}
+
+}  // namespace va
+
+extern "C" {
+
+va_status verify_attn_noalloc(const va_problem* p, const va_kv* kv, int32_t mode, float* o,
+                              float* lse, uint32_t* status, void* stream) {
+  va_status st = check(p, kv, mode);
+  if (st != VA_OK) return st;
+  if (p->total_rows == 0) return VA_OK;
+  if (!o || !lse) return VA_ERR_INVALID_ARG;
+  if (!aligned16(o)) return VA_ERR_ALIGNMENT;
+  Plan pl = make_plan(p, kv);
+  if (ws_bytes_for(p, kv, pl) > (size_t)VA_STATIC_WORKSPACE_BYTES)
+    return VA_ERR_WORKSPACE_TOO_SMALL;
+  void* ws = nullptr;
+  cudaError_t e = static_workspace(&ws);
+  if (e != cudaSuccess) return note_cuda(e);
+  Params q = make_params(p, kv, mode, pl, ws, o, lse, status);
+  cudaStream_t cs = (cudaStream_t)stream;
+  e = pl.kernel == 1 ? launch_umma_partial(q, pl.grid, cs) : launch_simt_partial(q, pl.grid, cs);
+  if (e != cudaSuccess) return note_cuda(e);
+  e = launch_merge(q, cs);
+  if (e != cudaSuccess) return note_cuda(e);
+  return VA_OK;
 }
 
 }  // extern "C"
