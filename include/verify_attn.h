@@ -114,15 +114,16 @@ typedef struct va_kv {
  *      row), 1 = tree; read in VA_MODE_MIXED only.
  *   Query head h reads KV head h / (num_heads / num_kv_heads).
  *   scale: softmax scale; 0 selects 1/sqrt(head_dim).
- *   num_splits: S >= 1.  Sequence s's span L = ctx + n is cut into S chunks
- *      of ceil(L/S) tokens rounded up to 16; each chunk writes an fp32
- *      online-softmax partial (possibly further cut into a fixed number of
- *      sub-chunks chosen from S, num_kv_heads and the GPU's SM count only),
- *      and a merge pass combines them in ascending order (hipfire PR #817,
- *      "Summary" and "Performance").  No choice depends on the other
- *      sequences of the launch, so a row's result depends only on its own
- *      sequence (lucebox PR #686, "Correctness failure found during
- *      qualification").
+ *   num_splits: S >= 1, the least number of KV chunks per sequence.
+ *      Sequence s's span L = ctx + n is cut into T equal chunks of
+ *      ceil(L/T') tokens rounded up to 16, T' = min(T, ceil(L/256)), where
+ *      T (>= S, <= 16 S) is fixed by S, num_kv_heads and the GPU's SM count
+ *      only (one wave of CTAs per sequence and KV head); each chunk writes
+ *      an fp32 online-softmax partial and a merge pass combines them in
+ *      ascending order (hipfire PR #817, "Summary" and "Performance").  No
+ *      choice depends on the other sequences of the launch, so a row's
+ *      result depends only on its own sequence (lucebox PR #686,
+ *      "Correctness failure found during qualification").
  */
 typedef struct va_problem {
   int32_t num_seqs;
@@ -205,8 +206,8 @@ va_status va_debug_gather_index(const va_problem *p, const va_kv *kv, int32_t kv
 /* Plan details for a problem (which kernel runs, splits and sub-splits). */
 typedef struct va_plan_info {
   int32_t kernel;          /* 0 = CUDA-core partial, 1 = tensor-core partial */
-  int32_t sub_splits;      /* P: sub-chunks per split */
-  int32_t slots;           /* S * P partial slots per (row, head) */
+  int32_t sub_splits;      /* T: KV chunks per sequence (equal to slots) */
+  int32_t slots;           /* T partial slots per (row, head) */
   int32_t grid_x, grid_y, grid_z;
   int32_t threads;
   int32_t smem_bytes;
@@ -249,8 +250,8 @@ va_status va_timing_read(int32_t max_calls, float *partial_ms, float *merge_ms,
  *
  * Limits and errors:
  *   - Problems whose va_workspace_size() exceeds VA_STATIC_WORKSPACE_BYTES
- *     (16 MiB: e.g. 32 split slots x 16 rows x 24 heads at D=256 fit,
- *     32 slots x 50 rows x 24 heads do not) return
+ *     (16 MiB: e.g. 38 slots x 16 rows x 24 heads at D=256 fit,
+ *     38 slots x 50 rows x 24 heads do not) return
  *     VA_ERR_WORKSPACE_TOO_SMALL before any launch; use the entry points
  *     with a caller workspace for those.
  *   - The first call on each device looks the scratch address up with

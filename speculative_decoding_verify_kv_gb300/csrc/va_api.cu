@@ -111,15 +111,18 @@ static Plan make_plan(const va_problem* p, const va_kv* kv) {
   pl.rows_per_block = tensor ? kUmmaRowsPerBlock : kSimtRowsPerBlock;
   pl.threads = tensor ? umma_threads(kv->head_dim, kv->dtype) : kSimtThreadsPerBlock;
   pl.smem = tensor ? umma_smem_bytes(kv->head_dim, kv->dtype) : simt_smem_bytes(kv->head_dim);
-  // Sub-chunks per split from S, the KV head count and the SM count only:
-  // never from the other sequences of the launch.  The tensor-core kernel
-  // holds one CTA per SM, the CUDA-core kernel about two.
+  // Each sequence's KV span is cut into `slots` equal 16-token-aligned
+  // chunks (fewer when the span is short), the count fixed by S, the KV
+  // head count and the SM count only: never by the other sequences of the
+  // launch.  One sequence's chunks of one KV head fill one wave of CTAs
+  // (the tensor-core kernel holds one CTA per SM, the CUDA-core kernel
+  // about two); the count is at least S and at most S * kMaxSubSplits.
   const int target = (tensor ? 1 : 2) * sm_count();
-  int P = target / (p->num_splits * kv->num_kv_heads);
-  if (P < 1) P = 1;
-  if (P > kMaxSubSplits) P = kMaxSubSplits;
-  pl.P = P;
-  pl.slots = p->num_splits * P;
+  int slots = target / kv->num_kv_heads;
+  if (slots < p->num_splits) slots = p->num_splits;
+  if (slots > p->num_splits * kMaxSubSplits) slots = p->num_splits * kMaxSubSplits;
+  pl.P = slots;
+  pl.slots = slots;
   const int rows = p->max_rows_per_seq * G;
   pl.row_blocks = (rows + pl.rows_per_block - 1) / pl.rows_per_block;
   pl.grid = dim3((unsigned)(pl.slots * pl.row_blocks), (unsigned)kv->num_kv_heads,
@@ -147,7 +150,7 @@ static Params make_params(const va_problem* p, const va_kv* kv, int mode, const 
   q.D = kv->head_dim;
   q.total_rows = p->total_rows;
   q.max_rows = p->max_rows_per_seq;
-  q.S = p->num_splits;
+  q.S = 1;  // one level of chunks: [0, L) in pl.slots pieces
   q.P = pl.P;
   q.slots = pl.slots;
   q.min_sub = kMinSubTokens;

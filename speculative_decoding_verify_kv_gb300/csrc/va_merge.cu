@@ -4,8 +4,8 @@
 // l_s and acc = sum 2^(m_s - M) acc_s, O = acc / l and LSE = (M + log2 l)
 // * ln 2.  A slot with l = 0 is an empty chunk and is skipped; a NaN slot
 // (device-detected error) makes the row NaN.  The summation order is fixed
-// (slot groups in ascending order, then groups in ascending order), so a
-// row's output depends only on its own slots.
+// (slots of a group in ascending order, then groups in ascending order), so
+// a row's output depends only on its own slots.
 //
 // Restated from hipfire PR #817 "FA2 split-KV" sections "Summary" and
 // "Performance" (S8 partials combined by a merge pass; S1 equals the
@@ -19,56 +19,37 @@ namespace va {
 
 constexpr int kMergeThreads = 256;
 
-// One CTA per (row, head).  Warp 0 finds M over the live slots; then D/4
-// column threads x (256 / (D/4)) slot groups accumulate float4 columns of
-// their slots, and the groups are added in fixed group order.
+// One CTA per (row, head): D/4 column threads x (256 / (D/4)) slot groups.
+// Group g takes slots g, g + NG, ... in ascending order and issues every
+// load of its slots (m, l and a float4 of acc) before using any, so the
+// merge costs one round trip to the partials.  Each group keeps its own
+// maximum M_g; the groups are then combined in ascending group order with
+// the overall maximum M:  l = sum_g 2^(M_g - M) l_g, acc likewise.
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
   constexpr int TC = D / 4;
   constexpr int NG = kMergeThreads / TC;
+  constexpr int BATCH = 12;  // slots per group loaded together
   __shared__ float4 red[NG][TC];
-  __shared__ float lred[NG];
-  __shared__ float M_s;
-  __shared__ int nan_s;
+  __shared__ float lred[NG], mred[NG];
   // Launched as a programmatic dependent of the partial kernel: wait here
   // until that grid has finished and its writes are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long item = blockIdx.x;
   const int grow = (int)(item / p.H), h = (int)(item % p.H);
   const int tcol = threadIdx.x % TC, grp = threadIdx.x / TC;
-  if (threadIdx.x < 32) {
-    float M = -INFINITY;
-    int nan = 0;
-    for (int sl = threadIdx.x; sl < p.slots; sl += 32) {
-      const long long si = slot_index(p, sl, grow, h);
-      const float m = p.ws_ml[2 * si], l = p.ws_ml[2 * si + 1];
-      if (isnan(m) || isnan(l)) nan = 1;
-      if (l > 0.f) M = fmaxf(M, m);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      nan |= __shfl_xor_sync(0xffffffffu, nan, o);
-    }
-    if (threadIdx.x == 0) {
-      M_s = M;
-      nan_s = nan;
-    }
-  }
-  __syncthreads();
-  const float M = M_s;
+  float Mg = -INFINITY, lg = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lsum = 0.f;
-  // Slots grp, grp+NG, ... in batches of 8 with every load of a batch in
-  // flight before any is used.
-  for (int s0 = grp; s0 < p.slots; s0 += 8 * NG) {
-    float mm[8], ll[8];
-    float4 aa[8];
+  int nan = 0;
+  for (int s0 = grp; s0 < p.slots; s0 += BATCH * NG) {
+    float mm[BATCH], ll[BATCH];
+    float4 aa[BATCH];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < BATCH; ++k) {
       const int sl = s0 + k * NG;
-      mm[k] = 0.f;
+      mm[k] = -INFINITY;
       ll[k] = 0.f;
+      aa[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (sl < p.slots) {
         const long long si = slot_index(p, sl, grow, h);
         mm[k] = p.ws_ml[2 * si];
@@ -76,11 +57,28 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
         aa[k] = *reinterpret_cast<const float4*>(p.ws_acc + si * D + 4 * tcol);
       }
     }
+    // A slot with l = 0 is an empty chunk (its acc is never read as data);
+    // a NaN (m, l) is a device-detected error and poisons the row.
+    float bm = Mg;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < BATCH; ++k) {
+      if (isnan(mm[k]) || isnan(ll[k])) nan = 1;
+      if (ll[k] > 0.f) bm = fmaxf(bm, mm[k]);
+    }
+    if (bm > Mg) {
+      const float f = exp2f(Mg - bm);  // 0 while nothing was live
+      lg *= f;
+      acc.x *= f;
+      acc.y *= f;
+      acc.z *= f;
+      acc.w *= f;
+      Mg = bm;
+    }
+#pragma unroll
+    for (int k = 0; k < BATCH; ++k) {
       if (!(ll[k] > 0.f)) continue;
-      const float w = exp2f(mm[k] - M);
-      lsum = fmaf(w, ll[k], lsum);
+      const float w = exp2f(mm[k] - Mg);
+      lg = fmaf(w, ll[k], lg);
       acc.x = fmaf(w, aa[k].x, acc.x);
       acc.y = fmaf(w, aa[k].y, acc.y);
       acc.z = fmaf(w, aa[k].z, acc.z);
@@ -88,26 +86,34 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
     }
   }
   red[grp][tcol] = acc;
-  if (tcol == 0) lred[grp] = lsum;
-  __syncthreads();
+  if (tcol == 0) {
+    lred[grp] = lg;
+    mred[grp] = Mg;
+  }
+  const bool bad = __syncthreads_or(nan) != 0;
   if (grp == 0) {
-    float4 t = red[0][tcol];
-    float lt = lred[0];
+    float M = -INFINITY;
 #pragma unroll
-    for (int g = 1; g < NG; ++g) {
+    for (int g = 0; g < NG; ++g)
+      if (lred[g] > 0.f) M = fmaxf(M, mred[g]);
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lt = 0.f;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      if (!(lred[g] > 0.f)) continue;
+      const float w = exp2f(mred[g] - M);
       const float4 b = red[g][tcol];
-      t.x += b.x;
-      t.y += b.y;
-      t.z += b.z;
-      t.w += b.w;
-      lt += lred[g];
+      t.x = fmaf(w, b.x, t.x);
+      t.y = fmaf(w, b.y, t.y);
+      t.z = fmaf(w, b.z, t.z);
+      t.w = fmaf(w, b.w, t.w);
+      lt = fmaf(w, lred[g], lt);
     }
-    const bool nan = nan_s != 0;
     const float inv = 1.f / lt;
-    float4 out = nan ? make_float4(NAN, NAN, NAN, NAN)
+    float4 out = bad ? make_float4(NAN, NAN, NAN, NAN)
                      : make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
     *reinterpret_cast<float4*>(p.o + item * D + 4 * tcol) = out;
-    if (tcol == 0) p.lse[item] = nan ? NAN : (M + log2f(lt)) * kLn2;
+    if (tcol == 0) p.lse[item] = bad ? NAN : (M + log2f(lt)) * kLn2;
   }
 }
 

@@ -60,9 +60,12 @@ struct UCfg {
   static constexpr int COL_Q = D + 2 * kNT;
   static constexpr int TMEM_COLS = (COL_Q + D / 2 <= 256) ? 256 : 512;
   static constexpr int DQ_WARPS = kQ8 ? 8 : 1;
-  // Q8: warps 10..19 minus 13 and 17, so that the MMA issuer's sub-partition
-  // (warp index = 1 mod 4) carries no dequantisation traffic.
-  static constexpr int THREADS = (kQ8 ? 20 : 11) * 32;
+  // Q8: dequantisation on warps 10..19 minus 13 and 17, so that the MMA
+  // issuers' sub-partition (warp index = 1 mod 4) carries none of it; warp
+  // 13 issues the P.V MMAs.  bf16: warp 10 fixes up V tails, warp 11 issues
+  // the P.V MMAs.
+  static constexpr int PV_WARP = kQ8 ? 13 : 11;
+  static constexpr int THREADS = (kQ8 ? 20 : 12) * 32;
   static constexpr int MAXREG = (65536 / THREADS) / 8 * 8 > 255 ? 255 : (65536 / THREADS) / 8 * 8;
   static constexpr int SMEM_Q8 = 2 * NB16 * TILE;
   static constexpr int SMEM_BF16 = NST * 2 * TILE;
@@ -73,23 +76,23 @@ struct UCfg {
 
 // Barrier slots in static shared memory.
 enum {
-  B_SFULL = 0,    // [2]
-  B_PFULL = 2,    // [2]
-  B_PVDONE = 4,
-  B_QREADY = 5,
-  B_DRAIN = 6,
-  B_OFINAL = 7,   // the last P.V has completed
+  B_SFULL = 0,    // [2] S of the buffer's tile is in TMEM
+  B_PFULL = 2,    // [2] P of the buffer's tile is in TMEM
+  B_SFREE = 4,    // [2] P.V of the buffer's tile has completed
+  B_QREADY = 6,
+  B_DRAIN = 7,    // [2] S issuer, P.V issuer
+  B_OFINAL = 9,   // the last P.V has completed
   // Q8 tile buffers, [tensor 0 = K / 1 = V][3]: raw bytes landed, fp16 ready,
   // buffer free again.
-  B_QFULL = 8,    // [2][3]
-  B_QREADY8 = 14, // [2][3]
-  B_QEMPTY = 20,  // [2][3]
+  B_QFULL = 10,   // [2][3]
+  B_QREADY8 = 16, // [2][3]
+  B_QEMPTY = 22,  // [2][3]
   // bf16 stages [NST]: K landed, V landed, V fixed up, stage free.
-  B_RFULL = 26,
-  B_VFULL = 34,
-  B_VREADY = 42,
-  B_REMPTY = 50,
-  B_COUNT = 58
+  B_RFULL = 28,
+  B_VFULL = 36,
+  B_VREADY = 44,
+  B_REMPTY = 52,
+  B_COUNT = 60
 };
 
 // Byte offset of element (row, col) inside one 128-byte-swizzled column
@@ -355,9 +358,11 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     mbar_init(bar(B_SFULL + 1), 1);
     mbar_init(bar(B_PFULL), 8);
     mbar_init(bar(B_PFULL + 1), 8);
-    mbar_init(bar(B_PVDONE), 1);
+    mbar_init(bar(B_SFREE), 1);
+    mbar_init(bar(B_SFREE + 1), 1);
     mbar_init(bar(B_QREADY), 8);
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_DRAIN + 1), 1);
     mbar_init(bar(B_OFINAL), 1);
     if (Q8) {
       for (int i = 0; i < 6; ++i) {
@@ -504,25 +509,69 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
+    // S(i) = Q K_i^T into S buffer i & 1, once K_i is ready and the P.V that
+    // last read that buffer (tile i - 2, whose P it held) has completed.
     if (lane == 0) {
       constexpr uint32_t ID_QK = idesc_f16(kM, kNT, !Q8, false);
-      constexpr uint32_t ID_PV = idesc_f16(kM, D, !Q8, true);
       bool ok = mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs);
       bool any = false;
-      auto issue_pv = [&](int t) -> bool {
-        const int bt = t & 1;
-        if (!mbar_wait(bar(B_PFULL + bt), (t >> 1) & 1, abort_p, kWaitNs)) return false;
-        uint32_t vaddr;
+      for (int i = 0; i < ntiles && ok; ++i) {
+        const int b = i & 1;
+        uint32_t kaddr;
         if (Q8) {
-          const int jb = t % C::NB16;
-          if (!mbar_wait(bar(B_QREADY8 + 3 + jb), (t / C::NB16) & 1, abort_p, kWaitNs)) return false;
-          vaddr = smem_u32(q8buf(1, jb));
+          const int jb = i % C::NB16;
+          ok = mbar_wait(bar(B_QREADY8 + jb), (i / C::NB16) & 1, abort_p, kWaitNs);
+          kaddr = smem_u32(q8buf(0, jb));
         } else {
+          const int st = i % C::NST;
+          ok = mbar_wait(bar(B_RFULL + st), (i / C::NST) & 1, abort_p, kWaitNs);
+          kaddr = smem_u32(kst(st));
+        }
+        if (ok && i >= 2)
+          ok = mbar_wait(bar(B_SFREE + b), ((i - 2) >> 1) & 1, abort_p, kWaitNs);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t kd0 = sdesc_sw128(kaddr, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * (kNT * 128) + (kk & 3) * 32) >> 4);
+          mma_ts(tm + C::COL_S0 + b * kNT, tm + C::COL_Q + kk * 8, kd, ID_QK, kk > 0 ? 1u : 0u);
+        }
+        any = true;
+        mma_commit(bar(B_SFULL + b));
+        if (Q8) mma_commit(bar(B_QEMPTY + i % C::NB16));
+      }
+      if (!ok) fail();
+      if (any) {
+        // Wait (bounded, regardless of abort) until these MMAs have finished.
+        int dummy = 0;
+        volatile int* never = &dummy;
+        mma_commit(bar(B_DRAIN));
+        mbar_wait(bar(B_DRAIN), 0, never, kWaitNs);
+      }
+    }
+  } else if (warp == C::PV_WARP) {
+    // ------------------------------------------------------------ P.V issuer
+    // O += P_t V_t once the softmax has written P_t (into S buffer t & 1)
+    // and V_t is ready; its completion frees the S buffer and V_t's buffer.
+    if (lane == 0) {
+      constexpr uint32_t ID_PV = idesc_f16(kM, D, !Q8, true);
+      bool ok = true, any = false;
+      for (int t = 0; t < ntiles && ok; ++t) {
+        const int bt = t & 1;
+        ok = mbar_wait(bar(B_PFULL + bt), (t >> 1) & 1, abort_p, kWaitNs);
+        uint32_t vaddr = 0;
+        if (ok && Q8) {
+          const int jb = t % C::NB16;
+          ok = mbar_wait(bar(B_QREADY8 + 3 + jb), (t / C::NB16) & 1, abort_p, kWaitNs);
+          vaddr = smem_u32(q8buf(1, jb));
+        } else if (ok) {
           const int st = t % C::NST;
-          if (!mbar_wait(bar(B_VREADY + st), (t / C::NST) & 1, abort_p, kWaitNs)) return false;
+          ok = mbar_wait(bar(B_VREADY + st), (t / C::NST) & 1, abort_p, kWaitNs);
           vaddr = smem_u32(vst(st));
         }
+        if (!ok) break;
         tc_fence_after();
         const uint32_t scol = tm + C::COL_S0 + bt * kNT;
         // Descriptor of the tile start; each 16-token K step adds 2048 bytes
@@ -535,49 +584,17 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
           if (!Q8) mma_ts(tm + C::COL_O, scol + kNT / 2 + kk * 8, vd, ID_PV, 1u);
         }
         any = true;
-        mma_commit(bar(B_PVDONE));
+        mma_commit(bar(B_SFREE + bt));
         if (Q8) mma_commit(bar(B_QEMPTY + 3 + t % C::NB16));
         else mma_commit(bar(B_REMPTY + t % C::NST));
-        return true;
-      };
-      if (ok) {
-        tc_fence_after();
-        for (int i = 0; i < ntiles && ok; ++i) {
-          const int b = i & 1;
-          uint32_t kaddr;
-          if (Q8) {
-            const int jb = i % C::NB16;
-            ok = mbar_wait(bar(B_QREADY8 + jb), (i / C::NB16) & 1, abort_p, kWaitNs);
-            kaddr = smem_u32(q8buf(0, jb));
-          } else {
-            const int st = i % C::NST;
-            ok = mbar_wait(bar(B_RFULL + st), (i / C::NST) & 1, abort_p, kWaitNs);
-            kaddr = smem_u32(kst(st));
-          }
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t kd0 = sdesc_sw128(kaddr, 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * (kNT * 128) + (kk & 3) * 32) >> 4);
-            mma_ts(tm + C::COL_S0 + b * kNT, tm + C::COL_Q + kk * 8, kd, ID_QK,
-                   kk > 0 ? 1u : 0u);
-          }
-          any = true;
-          mma_commit(bar(B_SFULL + b));
-          if (Q8) mma_commit(bar(B_QEMPTY + i % C::NB16));
-          if (i >= 1) ok = issue_pv(i - 1);
-        }
-        if (ok) ok = issue_pv(ntiles - 1);
-        if (ok) mma_commit(bar(B_OFINAL));
       }
+      if (ok) mma_commit(bar(B_OFINAL));
       if (!ok) fail();
       if (any) {
-        // Wait (bounded, regardless of abort) until our MMAs have finished.
         int dummy = 0;
         volatile int* never = &dummy;
-        mma_commit(bar(B_DRAIN));
-        mbar_wait(bar(B_DRAIN), 0, never, kWaitNs);
+        mma_commit(bar(B_DRAIN + 1));
+        mbar_wait(bar(B_DRAIN + 1), 0, never, kWaitNs);
       }
     }
   } else if (warp < 10) {
@@ -698,7 +715,8 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       const bool need = rvalid && (m_use != -INFINITY) && (mt > m_use + 8.f);
       const float m_new = (m_use == -INFINITY || need) ? mt : m_use;
       if (ok && __any_sync(0xffffffffu, need) &&
-          !__all_sync(0xffffffffu, mbar_wait(bar(B_PVDONE), (i - 1) & 1, abort_p, kWaitNs)))
+          !__all_sync(0xffffffffu, mbar_wait(bar(B_SFREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1,
+                                             abort_p, kWaitNs)))
         ok = false;
       if (ok && __any_sync(0xffffffffu, need)) {
         // Rescale this half of the warp's O rows once the previous P.V landed.
@@ -795,7 +813,8 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     // ------------------------------------------------------------ dequant / fix-up
     if (Q8 && (warp & 3) != 1) {
       // Warps 10, 11, 12, 14 dequantise K tiles, 15, 16, 18, 19 V tiles, each
-      // group at its own pace, in place in the tile buffers (13 and 17 idle).
+      // group at its own pace, in place in the tile buffers (warp 13 issues
+      // the P.V MMAs, 17 is idle).
       const int wq = warp - 10;
       const int dq = wq - (wq > 3) - (wq > 7);  // 0..7 over warps 10,11,12,14,15,16,18,19
       const int grp = dq >> 2;                  // 0 = K, 1 = V
