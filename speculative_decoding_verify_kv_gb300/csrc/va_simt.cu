@@ -15,6 +15,8 @@
 // "Performance" (split partials + merge), hipfire PR #695 alpineQ comments
 // (one block serves several verifier rows from one KV fetch), lucebox PR
 // #686 "State and commit invariants" (tree ancestry masks).
+#include <string.h>
+
 #include "va_common.cuh"
 
 namespace va {
@@ -42,6 +44,9 @@ __global__ void __launch_bounds__(kSimtThreads) simt_partial_kernel(const Params
 
   // The merge kernel may launch now; it waits for this grid to finish.
   asm volatile("griddepcontrol.launch_dependents;");
+  // Programmatic dependent of the preceding work on the stream: nothing is
+  // read or written before that work has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rb = blockIdx.x % p.row_blocks;
   const int sp = blockIdx.x / p.row_blocks;
@@ -192,7 +197,19 @@ static cudaError_t launch_simt_t(const Params& p, dim3 grid, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  simt_partial_kernel<D, KVT><<<grid, kSimtThreads, smem, st>>>(p);
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kSimtThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, simt_partial_kernel<D, KVT>, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -238,6 +238,10 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
 
   // The merge kernel may launch now; it waits for this grid to finish.
   asm volatile("griddepcontrol.launch_dependents;");
+  // Launched as a programmatic dependent of whatever precedes it on the
+  // stream: the CTAs may become resident early, but nothing is read or
+  // written before that work has completed and its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rb = blockIdx.x % p.row_blocks;
   const int sp = blockIdx.x / p.row_blocks;
@@ -934,7 +938,19 @@ static cudaError_t launch_umma_t(const Params& p, dim3 grid, cudaStream_t st) {
   if (!C::kQ8) {
     if (!make_map(&mk, p, p.k) || !make_map(&mv, p, p.v)) return cudaErrorInvalidValue;
   }
-  umma_partial_kernel<D, KVT><<<grid, C::THREADS, C::SMEM, st>>>(p, mk, mv);
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, umma_partial_kernel<D, KVT>, p, mk, mv);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
