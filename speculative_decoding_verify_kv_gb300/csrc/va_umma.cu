@@ -273,40 +273,6 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
   const int g = rvalid ? rseq % G : 0;
   const int kind = seq_kind_of(p, s);
 
-  if (tid == 0) {
-    err_s = 0;
-    abort_s = 0;
-  }
-  __syncthreads();
-  unsigned anc = 0;
-  if (rvalid && !err) {
-    bool bad = false;
-    anc = row_mask(kind, p.parent + row0, j, &bad);
-    if (bad) atomicOr(&err_s, (int)VA_DEV_BAD_PARENT);
-  }
-  if (!err && p.page_size != 0 && ntiles > 0) {
-    const int pg0 = slo / kPage, pg1 = (shi + kPage - 1) / kPage;
-    for (int pg = pg0 + tid; pg < pg1; pg += blockDim.x) {
-      int blk = p.block_table[(long long)s * p.max_blocks + pg];
-      if (blk < 0 || blk >= p.num_blocks) atomicOr(&err_s, (int)VA_DEV_BAD_BLOCK);
-    }
-  }
-  __syncthreads();
-  err |= (unsigned)err_s;
-
-  // Slot of this thread's row.
-  const int grow = row0 + j, h = kvh * G + g;
-  const long long si = slot_index(p, slot, grow, h);
-
-  if (err || ntiles == 0) {
-    if (err && tid == 0) flag(p.status, err);
-    if (rvalid) {
-      p.ws_ml[2 * si] = err ? NAN : -INFINITY;
-      p.ws_ml[2 * si + 1] = err ? NAN : 0.f;
-    }
-    return;
-  }
-
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
@@ -357,7 +323,19 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     }
   };
 
+  // Q8: tile 0 goes to buffers K0/V0, which the Q staging does not use.
+  // Contiguous cache: every address is known to be in range (the span was
+  // checked against the capacity), so these copies go out before the rest
+  // of the prologue.  Paged: after the block ids are checked.
+  auto issue_first = [&]() {
+    issue_q8(0, 0);
+    issue_q8(0, 1);
+  };
+  const bool early = Q8 && p.page_size == 0 && !err && ntiles > 0;
+
   if (tid == 0) {
+    err_s = 0;
+    abort_s = 0;
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_SFULL + 1), 1);
     mbar_init(bar(B_PFULL), 8);
@@ -383,35 +361,13 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       }
     }
     fence_barrier_init();
-    if (Q8) {
-      // Tile 0 goes to buffers K0/V0, which the Q staging does not use:
-      // start the HBM reads before the rest of the prologue.
-      issue_q8(0, 0);
-      issue_q8(0, 1);
-      for (int i = 1; i < min(kPrefetch, ntiles); ++i) {
-        prefetch_q8(i, 0);
-        prefetch_q8(i, 1);
-      }
-    }
+    if (early) issue_first();
   }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_base_s), C::TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tm = tmem_base_s;
-  volatile int* abort_p = &abort_s;
-  auto fail = [&]() {
-    *abort_p = 1;
-    flag(p.status, VA_DEV_TIMEOUT);
-  };
-
-
   // Q8: warps 2.. stage this CTA's Q rows in shared memory (tile buffers
-  // K1 onwards) with every load in flight; the softmax warps convert them
-  // into TMEM, and the producer loads tile 1 there only after Q is ready.
+  // K1 onwards; rows padded to kQRow bytes so that the lanes of a warp read
+  // distinct bank groups) with every load in flight, overlapping the rest of
+  // the prologue; the softmax warps convert them into TMEM, and the
+  // producer loads tile 1 there only after Q is ready.
   constexpr int kQRow = D * 2 + 16;
   if (Q8 && warp >= 2) {
     constexpr int CPR = D / 8;  // 16-byte chunks per row
@@ -438,6 +394,58 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     }
     named_barrier_sync(2, NTHR);
   }
+  __syncthreads();
+  unsigned anc = 0;
+  if (rvalid && !err) {
+    bool bad = false;
+    anc = row_mask(kind, p.parent + row0, j, &bad);
+    if (bad) atomicOr(&err_s, (int)VA_DEV_BAD_PARENT);
+  }
+  if (!err && p.page_size != 0 && ntiles > 0) {
+    const int pg0 = slo / kPage, pg1 = (shi + kPage - 1) / kPage;
+    for (int pg = pg0 + tid; pg < pg1; pg += blockDim.x) {
+      int blk = p.block_table[(long long)s * p.max_blocks + pg];
+      if (blk < 0 || blk >= p.num_blocks) atomicOr(&err_s, (int)VA_DEV_BAD_BLOCK);
+    }
+  }
+  __syncthreads();
+  err |= (unsigned)err_s;
+
+  // Slot of this thread's row.
+  const int grow = row0 + j, h = kvh * G + g;
+  const long long si = slot_index(p, slot, grow, h);
+
+  if (err || ntiles == 0) {
+    if (early && tid == 0) {
+      // Let the copies already issued land before the CTA goes away.
+      int dummy = 0;
+      volatile int* never = &dummy;
+      mbar_wait(bar(B_QFULL), 0, never, kWaitNs);
+      mbar_wait(bar(B_QFULL + 3), 0, never, kWaitNs);
+    }
+    if (err && tid == 0) flag(p.status, err);
+    if (rvalid) {
+      p.ws_ml[2 * si] = err ? NAN : -INFINITY;
+      p.ws_ml[2 * si + 1] = err ? NAN : 0.f;
+    }
+    return;
+  }
+
+  if (Q8 && !early && tid == 0) issue_first();
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_s), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = tmem_base_s;
+  volatile int* abort_p = &abort_s;
+  auto fail = [&]() {
+    *abort_p = 1;
+    flag(p.status, VA_DEV_TIMEOUT);
+  };
+
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -445,6 +453,14 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       const uint64_t pol = policy_evict_first();
       int issued = Q8 ? 1 : 0;
       if (Q8) {
+        // L2 prefetches of tiles 1.. once tile 0 (whose HBM reads they would
+        // otherwise compete with) has landed.
+        if (ntiles > 1 && mbar_wait(bar(B_QFULL), 0, abort_p, kWaitNs)) {
+          for (int i = 1; i < min(kPrefetch, ntiles); ++i) {
+            prefetch_q8(i, 0);
+            prefetch_q8(i, 1);
+          }
+        }
         // Buffers K1.. hold the Q staging until the softmax warps have put
         // Q into TMEM.
         if (ntiles > 1 && !mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs)) fail();
