@@ -800,34 +800,35 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     }
     // O rows go through shared memory (the tile buffers are idle now; rows
     // padded by 16 bytes so a warp's stores hit distinct bank groups) and
-    // leave as one 16-byte-aligned bulk copy per row.
+    // leave row by row with coalesced warp-wide stores.
     constexpr int kORow = D * 4 + 16;
     if (!bad && warp_live) {
 #pragma unroll 1
-      for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 16) {
-        uint32_t o[16];
-        tmem_ld16(tm + lane_base + C::COL_O + c0, o);
+      for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tm + lane_base + C::COL_O + c0, o);
         tmem_wait_ld();
         if (rvalid) {
 #pragma unroll
-          for (int c = 0; c < 16; c += 4)
+          for (int c = 0; c < 32; c += 4)
             *reinterpret_cast<uint4*>(sm + r * kORow + (c0 + c) * 4) =
                 make_uint4(o[c], o[c + 1], o[c + 2], o[c + 3]);
         }
       }
     }
-    fence_proxy_async_smem();
     named_barrier_sync(1, 256);
-    if (!bad && lane == 0) {
-      // Warp w stores rows w - 2, w + 6, ... (eight warps share the rows).
+    if (!bad) {
+      // Warp w copies rows w - 2, w + 6, ... (eight warps share the rows),
+      // each row with whole-warp 16-byte stores (coalesced 512-byte runs).
       const int nrows_blk = min(kM, R - rb * kM);
       for (int rr = warp - 2; rr < nrows_blk; rr += 8) {
         const int rs2 = rb * kM + rr;
         const long long si2 = slot_index(p, slot, row0 + rs2 / G, kvh * G + rs2 % G);
-        bulk_s2g(p.ws_acc + si2 * D, smem_u32(sm + rr * kORow), D * 4);
+        const uint4* srow = reinterpret_cast<const uint4*>(sm + rr * kORow);
+        uint4* grow4 = reinterpret_cast<uint4*>(p.ws_acc + si2 * D);
+#pragma unroll
+        for (int c = lane; c < D / 4; c += 32) grow4[c] = srow[c];
       }
-      bulk_commit();
-      bulk_wait_all();
     }
   } else {
     // ------------------------------------------------------------ dequant / fix-up
