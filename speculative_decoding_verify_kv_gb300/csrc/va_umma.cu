@@ -622,7 +622,8 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     // Warps 2..9: quad = warp & 3 selects the TMEM lane quadrant (32 rows),
     // half = (warp - 2) >> 2 selects which 32 of the tile's 64 columns this
     // thread scores; the two halves of a row exchange their maxima through
-    // shared memory once per tile.
+    // shared memory once per tile (named barrier 5 + quad: just the two
+    // warps of the quadrant).
     const int half = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const bool warp_live = __any_sync(0xffffffffu, rvalid);
@@ -656,7 +657,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
           }
         }
         red_q[half][r] = amax;
-        named_barrier_sync(1, 256);
+        named_barrier_sync(5 + quad, 64);  // the row's two halves
         amax = fmaxf(amax, red_q[half ^ 1][r]);
         int e = 0;
         if (amax > 0.f) frexpf(amax, &e);
@@ -729,7 +730,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       }
       // Row maximum over both halves (raw scores; c_r > 0).
       red_max[b][half][r] = mx;
-      named_barrier_sync(1, 256);
+      named_barrier_sync(5 + quad, 64);  // the row's two halves
       mx = fmaxf(mx, red_max[b][half ^ 1][r]);
       const float mt = mx * c_r;
       const bool need = rvalid && (m_use != -INFINITY) && (mt > m_use + 8.f);
@@ -792,7 +793,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     if (!ok && lane == 0) fail();
     tc_fence_after();
     if (half == 1) red_l[r] = l_run;
-    named_barrier_sync(1, 256);
+    named_barrier_sync(5 + quad, 64);  // the row's two halves
     const bool bad = __any_sync(0xffffffffu, *abort_p != 0);
     if (rvalid && half == 0) {
       p.ws_ml[2 * si] = bad ? NAN : m_use;
