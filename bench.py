@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kernel", default="auto", choices=["auto", "cuda-cores"])
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other verify workloads (reported under 'workloads')")
     ap.add_argument("--profile", action="store_true",
                     help="profiling run for ncu: W + K eager calls of the headline workload "
                          "(--ctx selects the context), no graphs, no JSON line")
@@ -491,6 +493,29 @@ def run_ours(args):
                               "merge_us": float(np.mean(mm)) * 1e3}
         del b2
 
+    # The other verify workloads (context for the headline; same method:
+    # rotating KV copies >= 3x L2, graphs of library calls, CUDA events).
+    workloads = {}
+    if not args.no_workloads:
+        for name, make in [("dflash-bf16 ctx4096 S8", lambda: sy.dflash_bf16(ctx=4096, num_splits=8)),
+                           ("dflash-bf16 ctx8192 S8", lambda: sy.dflash_bf16(ctx=8192, num_splits=8)),
+                           ("paged-d128 bf16 4x~29K S8", lambda: sy.paged_d128()),
+                           ("mixed tree+direct Q8 paged S8", lambda: sy.mixed_tree_direct())]:
+            c3 = make()
+            b3 = Bench(c3, flags, l2)
+            for i in range(3):
+                b3.call(i)
+            b3.capture(2 * b3.copies)
+            n3 = max(2 * b3.copies, min(args.steps, 200) // (2 * b3.copies) * (2 * b3.copies))
+            ms3 = max_over_ranks(b3.timed(n3, world), world)
+            us = ms3 / n3 * 1e3
+            workloads[name] = {"us_per_call": us, "kv_bytes_per_call": c3.kv_bytes,
+                               "kv_gbs": c3.kv_bytes / (us * 1e-6) / 1e9,
+                               "hbm_frac": c3.kv_bytes / (us * 1e-6) / 1e9 / peak,
+                               "kernel": "tensor-core" if b3.plan["kernel"] == 1 else "CUDA-core",
+                               "slots": b3.plan["slots"]}
+            del b3
+
     e2e = None
     if not args.no_e2e:
         e2e = e2e_measure(case, steps=max(3, min(args.steps, 50)), warmup=3, flags=flags)
@@ -522,6 +547,7 @@ def run_ours(args):
         "us_per_call_instrumented": ms_instr / args.steps * 1e3,
         "hbm_frac_call": value / world / peak,
         "contexts": contexts,
+        "workloads": workloads,
         "roofline": {"kernel": kernel_name, "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak if achieved else None,
                      "traffic": profiled_traffic() if b.plan["kernel"] == 1 else None,
