@@ -458,6 +458,7 @@ def run_ours(args):
         torch.cuda.synchronize()
     ms = b.timed(args.steps, world)
     ms_instr = b.timed(args.steps, world, instrumented=True)
+    assert int(b.status.item()) == 0, f"device status {int(b.status.item()):#x} in the timed region"
     partial_ms, merge_ms = va.timing_read(calls_per_graph)
     t_end = time.time() + 0.5
     while time.time() < t_end:
@@ -485,6 +486,7 @@ def run_ours(args):
         b2.capture(4 * b2.copies)
         n2 = max(4 * b2.copies, min(args.steps, 400))
         ms2 = max_over_ranks(b2.timed(n2, world), world)
+        assert int(b2.status.item()) == 0, f"ctx {ctx}: device status {int(b2.status.item()):#x}"
         b2.timed(n2, world, instrumented=True)
         pm, mm = va.timing_read(4 * b2.copies)
         us = ms2 / n2 * 1e3
@@ -508,6 +510,7 @@ def run_ours(args):
             b3.capture(2 * b3.copies)
             n3 = max(2 * b3.copies, min(args.steps, 200) // (2 * b3.copies) * (2 * b3.copies))
             ms3 = max_over_ranks(b3.timed(n3, world), world)
+            assert int(b3.status.item()) == 0, f"{name}: device status {int(b3.status.item()):#x}"
             us = ms3 / n3 * 1e3
             workloads[name] = {"us_per_call": us, "kv_bytes_per_call": c3.kv_bytes,
                                "kv_gbs": c3.kv_bytes / (us * 1e-6) / 1e9,
