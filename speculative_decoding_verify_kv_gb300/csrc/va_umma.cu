@@ -105,6 +105,115 @@ __device__ __forceinline__ void named_barrier_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Q8_0 dequantisation by direct loads (paged caches).  A thread owns one
+// half-row (token t = gtid % 64 of the tile, half hf = gtid / 64 of its
+// D/32 blocks).  It loads the raw bytes of its half-row from global memory
+// into registers (DqRaw, issued before the tile buffer is free, so the
+// latency hides behind the wait), then converts them and writes fp16 into
+// the 128-byte-swizzled K-major tile layout (eight consecutive threads take
+// eight consecutive tokens of one block, so their 16-byte stores hit
+// distinct bank groups).  Tokens >= valid become zeros.
+template <int D>
+struct DqRaw {
+  static constexpr int NB = D / 32;               // blocks per row
+  static constexpr int RB = NB * 34;              // bytes per row
+  static constexpr int HB = RB / 2;               // bytes per half-row
+  // D = 256: nine 16-byte loads per half, the second half starting 8 bytes
+  // early (both stay inside the row).  Otherwise: 4-byte loads from the word
+  // at or below the first byte.
+  static constexpr int NW = D == 256 ? 36 : (HB + (HB % 4 ? 2 : 0) + 3) / 4;
+  uint32_t w[NW];
+};
+
+// `row` is in global memory (read-only for the kernel's lifetime).
+template <int D>
+__device__ __forceinline__ void dq_load(DqRaw<D>& r, const unsigned char* row, int hf, bool live) {
+  using R = DqRaw<D>;
+  if (!live) return;
+  if (D == 256) {
+    const uint4* q = reinterpret_cast<const uint4*>(row + (hf ? R::HB - 8 : 0));
+#pragma unroll
+    for (int k = 0; k < 9; ++k) {
+      const uint4 v = __ldg(q + k);
+      r.w[4 * k] = v.x;
+      r.w[4 * k + 1] = v.y;
+      r.w[4 * k + 2] = v.z;
+      r.w[4 * k + 3] = v.w;
+    }
+  } else {
+    const int start = hf * R::HB;
+    const uint32_t* q = reinterpret_cast<const uint32_t*>(row + (start & ~3));
+#pragma unroll
+    for (int k = 0; k < R::NW; ++k) r.w[k] = __ldg(q + k);
+  }
+}
+
+// Convert and store; SH = byte offset of the half-row's first block within
+// the loaded words.
+template <int D, int SH>
+__device__ __forceinline__ void dq_store(const DqRaw<D>& r, unsigned char* buf, int t, int hf,
+                                         bool live) {
+  constexpr int NBH = D / 64;                     // blocks per half-row
+#pragma unroll
+  for (int jb = 0; jb < NBH; ++jb) {
+    const int b = hf * NBH + jb;                  // block index in the row
+    unsigned char* drow = buf + (b >> 1) * (kNT * 128);
+    const int c0 = (b & 1) * 4;
+    uint4 out[4];
+    if (live) {
+      constexpr int O0 = SH;
+      const int o = O0 + 34 * jb;                 // block offset in the loaded bytes
+      const int wo = o >> 2;
+      uint32_t sbits, code[8];
+      if (o & 2) {
+        sbits = r.w[wo] >> 16;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) code[q] = r.w[wo + 1 + q];
+      } else {
+        sbits = r.w[wo] & 0xFFFFu;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) code[q] = __funnelshift_r(r.w[wo + q], r.w[wo + q + 1], 16);
+      }
+      const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)sbits));
+      const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
+      uint32_t hv[16];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t x = code[q] ^ 0x80808080u;  // bytes q + 128
+        uint32_t lo = __byte_perm(x, 0x64646464u, 0x4140);
+        uint32_t hi = __byte_perm(x, 0x64646464u, 0x4342);
+        __half2 a = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&lo), bias), d2);
+        __half2 c = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&hi), bias), d2);
+        hv[2 * q] = *reinterpret_cast<uint32_t*>(&a);
+        hv[2 * q + 1] = *reinterpret_cast<uint32_t*>(&c);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        out[c] = make_uint4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) out[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4*>(drow + sw128_off(t, c0 + c)) = out[c];
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void dq_convert(const DqRaw<D>& r, unsigned char* buf, int t, int hf,
+                                           bool live) {
+  if (D == 256) {
+    if (hf) dq_store<D, 8>(r, buf, t, hf, live);
+    else dq_store<D, 0>(r, buf, t, hf, live);
+  } else {
+    // 4-byte loads: the half-row starts 0 or 2 bytes into the first word.
+    const int sh = (hf * DqRaw<D>::HB) & 3;
+    if (sh) dq_store<D, 2>(r, buf, t, hf, live);
+    else dq_store<D, 0>(r, buf, t, hf, live);
+  }
+}
+
 // Dequantise, in place, the raw Q8_0 rows (RB bytes apart) at the start of
 // a tile buffer into the fp16 MMA layout of the same buffer; tokens >= valid
 // become zeros.  128 threads (named barrier `barid`): thread -> (token
@@ -221,7 +330,10 @@ __device__ __forceinline__ void pack_p(float a, float b, uint32_t& hi, uint32_t&
   }
 }
 
-template <int D, int KVT>
+// PAGED (Q8 only): the cache is paged and the dequantising warps load the
+// raw rows themselves; a separate instantiation, so the contiguous kernel
+// carries none of that code.
+template <int D, int KVT, bool PAGED>
 __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D, KVT>::MAXREG))
     umma_partial_kernel(const Params p, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV) {
@@ -323,10 +435,14 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     }
   };
 
-  // Q8: tile 0 goes to buffers K0/V0, which the Q staging does not use.
-  // Contiguous cache: every address is known to be in range (the span was
-  // checked against the capacity), so these copies go out before the rest
-  // of the prologue.  Paged: after the block ids are checked.
+  // Q8, contiguous cache: the raw rows of a tile arrive by one bulk copy per
+  // tensor into the tile buffer and are dequantised in place.  Paged cache:
+  // a tile would take one small copy per 16-token page, so the dequantising
+  // warps load the raw rows themselves (`direct`).  Tile 0 goes to buffers
+  // K0/V0, which the Q staging does not use; every address is known to be in
+  // range (the span was checked against the capacity), so these copies go
+  // out before the rest of the prologue.
+  constexpr bool direct = Q8 && PAGED;
   auto issue_first = [&]() {
     issue_q8(0, 0);
     issue_q8(0, 1);
@@ -431,7 +547,6 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     return;
   }
 
-  if (Q8 && !early && tid == 0) issue_first();
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_base_s), C::TMEM_COLS);
     tmem_relinquish();
@@ -452,7 +567,9 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int issued = Q8 ? 1 : 0;
-      if (Q8) {
+      if (direct) {
+        issued = 0;  // nothing to copy: the dequantising warps load the rows
+      } else if (Q8) {
         // L2 prefetches of tiles 1.. once tile 0 (whose HBM reads they would
         // otherwise compete with) has landed.
         if (ntiles > 1 && mbar_wait(bar(B_QFULL), 0, abort_p, kWaitNs)) {
@@ -516,7 +633,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
         }
       }
       // Drain: make sure no copy of ours is still landing in shared memory.
-      if (*abort_p) {
+      if (!direct && *abort_p) {
         int dummy = 0;
         volatile int* never = &dummy;
         const int nslot = Q8 ? C::NB16 : C::NST;
@@ -833,7 +950,52 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     }
   } else {
     // ------------------------------------------------------------ dequant / fix-up
-    if (Q8 && (warp & 3) != 1) {
+    if (direct && (warp & 3) != 1) {
+      // Paged Q8: warps 10, 11, 12, 14 dequantise K tiles, 15, 16, 18, 19 V
+      // tiles, each group at its own pace (warp 13 issues the P.V MMAs, 17
+      // is idle).  Per tile: load the raw half-row from global memory, wait
+      // until the tile buffer is free (the MMA that read its previous tile
+      // has completed; tiles 1 and 2 also wait for Q to have left the
+      // staging area), convert, store, release.
+      const int wq = warp - 10;
+      const int dq = wq - (wq > 3) - (wq > 7);  // 0..7 over warps 10,11,12,14,15,16,18,19
+      const int grp = dq >> 2;                  // 0 = K, 1 = V
+      const int gtid = (dq & 3) * 32 + lane;
+      const int t = gtid & 63, hf = gtid >> 6;
+      const unsigned char* src = reinterpret_cast<const unsigned char*>(grp ? p.v : p.k);
+      // A failed wait does not leave the loop (no named barrier here, but
+      // the stores must stay out of buffers an MMA may still read).
+      bool ok = true;
+      for (int i = 0; i < ntiles; ++i) {
+        const int jb = i % C::NB16;
+        const int t0 = slo + i * kNT;
+        const int tok = t0 + t;
+        const bool live = ok && tok < shi;
+        const int blk = live ? p.block_table[(long long)s * p.max_blocks + tok / kPage] : 0;
+        const unsigned char* row =
+            src + (((long long)blk * p.KVH + kvh) * kPage + tok % kPage) * C::RB;
+        DqRaw<D> raw;
+        dq_load<D>(raw, row, hf, live);
+        // The group's first thread keeps its tensor kPrefetch tiles ahead in
+        // L2 (tiles 1..kPrefetch once tile 0's reads are out).
+        if (gtid == 0) {
+          const int lo_i = i == 0 ? 1 : i + kPrefetch, hi_i = min(i + kPrefetch + 1, ntiles);
+          for (int k = lo_i; k < hi_i; ++k) prefetch_q8(k, grp);
+        }
+        if (ok && !__all_sync(0xffffffffu,
+                              mbar_wait(bar(B_QEMPTY + 3 * grp + jb), ((i / C::NB16) & 1) ^ 1,
+                                        abort_p, kWaitNs) &&
+                                  (i == 0 || mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs)))) {
+          ok = false;
+          if (lane == 0) fail();
+        }
+        if (!ok) continue;
+        dq_convert<D>(raw, q8buf(grp, jb), t, hf, live);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_QREADY8 + 3 * grp + jb));
+      }
+    } else if (Q8 && (warp & 3) != 1) {
       // Warps 10, 11, 12, 14 dequantise K tiles, 15, 16, 18, 19 V tiles, each
       // group at its own pace, in place in the tile buffers (warp 13 issues
       // the P.V MMAs, 17 is idle).
@@ -940,12 +1102,12 @@ static bool make_map(CUtensorMap* map, const Params& p, const void* base) {
   return r == CUDA_SUCCESS;
 }
 
-template <int D, int KVT>
+template <int D, int KVT, bool PAGED>
 static cudaError_t launch_umma_t(const Params& p, dim3 grid, cudaStream_t st) {
   using C = UCfg<D, KVT>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(umma_partial_kernel<D, KVT>,
+    cudaError_t e = cudaFuncSetAttribute(umma_partial_kernel<D, KVT, PAGED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
@@ -967,7 +1129,7 @@ static cudaError_t launch_umma_t(const Params& p, dim3 grid, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, umma_partial_kernel<D, KVT>, p, mk, mv);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, umma_partial_kernel<D, KVT, PAGED>, p, mk, mv);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -987,11 +1149,15 @@ int umma_smem_bytes(int D, int kv_dtype) {
 }
 
 cudaError_t launch_umma_partial(const Params& p, dim3 grid, cudaStream_t st) {
-#define VA_U_CASE(DD, KT) \
-  if (p.D == DD && p.kv_dtype == KT) return launch_umma_t<DD, KT>(p, grid, st);
-  VA_U_CASE(64, VA_BF16) VA_U_CASE(64, VA_Q8_0) VA_U_CASE(128, VA_BF16)
-  VA_U_CASE(128, VA_Q8_0) VA_U_CASE(256, VA_BF16) VA_U_CASE(256, VA_Q8_0)
-#undef VA_U_CASE
+#define VA_U_BF16(DD) \
+  if (p.D == DD && p.kv_dtype == VA_BF16) return launch_umma_t<DD, VA_BF16, false>(p, grid, st);
+#define VA_U_Q8(DD)                                                                       \
+  if (p.D == DD && p.kv_dtype == VA_Q8_0)                                                 \
+    return p.page_size != 0 ? launch_umma_t<DD, VA_Q8_0, true>(p, grid, st)              \
+                            : launch_umma_t<DD, VA_Q8_0, false>(p, grid, st);
+  VA_U_BF16(64) VA_U_Q8(64) VA_U_BF16(128) VA_U_Q8(128) VA_U_BF16(256) VA_U_Q8(256)
+#undef VA_U_BF16
+#undef VA_U_Q8
   return cudaErrorInvalidValue;
 }
 
