@@ -71,13 +71,29 @@ def test_mixed_small(flags):
     full(c, flags)
 
 
+@pytest.mark.parametrize("paged", [False, True])
 @pytest.mark.parametrize("kv_dtype", [sy.BF16, sy.Q8_0])
 @pytest.mark.parametrize("D", [64, 128])
-def test_other_head_dims(kv_dtype, D):
+def test_other_head_dims(kv_dtype, D, paged):
     c = sy.make_case(f"d{D}", num_heads=8, num_kv_heads=2, head_dim=D, kv_dtype=kv_dtype,
                      q_dtype=sy.BF16, ctx=[200, 7], rows=[5, 3], kinds=[1, 0], mode="mixed",
-                     paged=True, seed=205 + D)
+                     paged=paged, seed=205 + D)
     full(c, 0, 3)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_q8_paged_equals_contiguous_bitwise_multi_tile(D):
+    """The paged Q8 kernel loads raw rows itself while the contiguous one
+    lands them by bulk copy and dequantises in place: same arithmetic, so
+    the same bits, over several tiles and a ragged tail."""
+    kw = dict(num_heads=8, num_kv_heads=2, head_dim=D, kv_dtype=sy.Q8_0, q_dtype=sy.BF16,
+              ctx=[700, 333], rows=[7, 2], seed=230 + D)
+    cp = sy.make_case(f"q8-paged-d{D}", paged=True, extra_blocks=3, **kw)
+    cc = sy.to_contiguous(cp)
+    op, lp = _gpu(cp, 2)
+    oc, lc = _gpu(cc, 2)
+    assert np.array_equal(op, oc) and np.array_equal(lp, lc)
+    full(cp, 0, 2)
 
 
 def test_f32_cache_bf16_query():
