@@ -35,7 +35,7 @@ cudaError_t launch_debug_gather(const Params& p, int kvh, long long max_len, lon
 constexpr int kSimtRowsPerBlock = 16;
 constexpr int kSimtThreadsPerBlock = 128;
 constexpr int kUmmaRowsPerBlock = 128;
-constexpr int kMinSubTokens = 256;
+constexpr int kMinSubTokens = 128;
 constexpr int kMaxSubSplits = 16;
 
 static int sm_count() {

@@ -12,6 +12,7 @@
 namespace va {
 
 constexpr int kPage = 16;
+constexpr int kChunkAlign = 64;  // KV chunks are whole 64-token tiles
 constexpr int kQ8Block = 32;
 constexpr int kQ8BlockBytes = 34;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -64,18 +65,16 @@ __device__ __forceinline__ void split_range(int L, int S, int s, int* lo, int* h
   *hi = (int)(b < L ? b : L);
 }
 
+// Chunk p of [lo, hi) cut into at most P chunks of a whole number of
+// 64-token tiles, each at least min_sub tokens: the chunk length is
+// ceil((hi - lo) / P) (or min_sub if larger) rounded up to 64; chunks past
+// the end are empty.
 __device__ __forceinline__ void sub_range(int lo, int hi, int P, int min_sub, int p, int* slo,
                                           int* shi) {
-  int len = hi - lo;
-  int live = (len + min_sub - 1) / min_sub;
-  if (live > P) live = P;
-  if (live < 1) live = 1;
-  if (p >= live) {
-    *slo = *shi = hi;
-    return;
-  }
-  int per = (len + live - 1) / live;
-  int sub = (per + kPage - 1) / kPage * kPage;
+  const int len = hi - lo;
+  int per = (len + P - 1) / P;
+  if (per < min_sub) per = min_sub;
+  const int sub = (per + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
   long long a = lo + (long long)p * sub, b = lo + (long long)(p + 1) * sub;
   *slo = (int)(a < hi ? a : hi);
   *shi = (int)(b < hi ? b : hi);
