@@ -114,16 +114,16 @@ typedef struct va_kv {
  *      row), 1 = tree; read in VA_MODE_MIXED only.
  *   Query head h reads KV head h / (num_heads / num_kv_heads).
  *   scale: softmax scale; 0 selects 1/sqrt(head_dim).
- *   num_splits: S >= 1, the least number of KV chunks per sequence.
- *      Sequence s's span L = ctx + n is cut into T equal chunks of
- *      ceil(L/T') tokens rounded up to 16, T' = min(T, ceil(L/256)), where
- *      T (>= S, <= 16 S) is fixed by S, num_kv_heads and the GPU's SM count
- *      only (one wave of CTAs per sequence and KV head); each chunk writes
- *      an fp32 online-softmax partial and a merge pass combines them in
- *      ascending order (hipfire PR #817, "Summary" and "Performance").  No
- *      choice depends on the other sequences of the launch, so a row's
- *      result depends only on its own sequence (lucebox PR #686,
- *      "Correctness failure found during qualification").
+ *   num_splits: S >= 1.  Sequence s's span L = ctx + n is cut into chunks
+ *      of max(ceil(L/T), 128) tokens rounded up to a whole number of
+ *      64-token tiles (at most T chunks), where T (>= S, <= 16 S) is fixed
+ *      by S, num_kv_heads and the GPU's SM count only (one wave of CTAs per
+ *      sequence and KV head); each chunk writes an fp32 online-softmax
+ *      partial and a merge pass combines them in ascending order (hipfire
+ *      PR #817, "Summary" and "Performance").  No choice depends on the
+ *      other sequences of the launch, so a row's result depends only on
+ *      its own sequence (lucebox PR #686, "Correctness failure found during
+ *      qualification").
  */
 typedef struct va_problem {
   int32_t num_seqs;
