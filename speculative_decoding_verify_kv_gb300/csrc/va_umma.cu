@@ -1,14 +1,16 @@
 // Tensor-core split-KV partial kernel (tcgen05 + TMEM + TMA), sm_103a.
 //
-// One CTA owns (sequence, KV head, split, sub-chunk) and ALL query rows of
-// that KV head (n rows x G heads <= 128), so every K/V byte of its token
-// range is read from HBM exactly once for every row it serves (hipfire PR
-// #695, alpineQ comments: one block reuses each Q8 K/V fetch across several
-// verifier rows; here across all of them).  Per 64-token tile:
+// One CTA owns (sequence, KV head, KV chunk) and ALL query rows of that KV
+// head (n rows x G heads <= 128 per row block), so every K/V byte of its
+// token range is read from HBM exactly once for every row it serves
+// (hipfire PR #695, alpineQ comments: one block reuses each Q8 K/V fetch
+// across several verifier rows; here across all of them).  Per 64-token
+// tile:
 //
 //   S = Q K^T      tcgen05.mma, A = Q (TMEM), B = K tile (smem, K-major)
-//   softmax        4 warps, one TMEM lane (= query row) per thread; masks;
-//                  online (m, l) in log2 units; P written back over S
+//   softmax        8 warps, one TMEM lane (= query row) per thread and one
+//                  half of the tile's columns per warp; masks; online
+//                  (m, l) in log2 units; P written back over S
 //   O += P V       tcgen05.mma, A = P (TMEM), B = V tile (smem, MN-major)
 //
 // O (fp32, 128 lanes x D columns) lives in TMEM for the CTA's whole range.
@@ -17,19 +19,22 @@
 // and "Performance").
 //
 // Caches:
-//   Q8_0: raw 34-byte blocks arrive by 1-D bulk TMA into a staging ring;
-//     8 warps dequantise them to fp16 (one rounding of d*q) straight into
-//     the 128-byte-swizzled MMA layout, zero-filling tokens past the range.
-//     Q is converted to fp16 after a per-row power-of-two rescale (exact),
-//     and the scale folds into the score multiplier.  P is fp16.
+//   Q8_0, contiguous: a tile's raw 34-byte blocks arrive by one 1-D bulk
+//     copy per tensor into a tile buffer; four warps per tensor dequantise
+//     them in place to fp16 (one rounding of d*q) in the 128-byte-swizzled
+//     MMA layout, zero-filling tokens past the range.  Paged (a separate
+//     instantiation): the same warps load the raw rows themselves through
+//     the block table.  Q is converted to fp16 after a per-row power-of-two
+//     rescale (exact), and the scale folds into the score multiplier.  P
+//     is fp16.
 //   bf16: tiled TMA loads place K/V tiles directly in the MMA layout; one
 //     warp zeroes V rows past the range of a ragged tile.  P is split into
 //     bf16 hi + lo halves (two MMAs) so P keeps 16 significant bits.
 //
-// Warp roles: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 2..9 =
-// softmax/epilogue (two warps per TMEM lane quadrant, one per half of the
-// tile's columns), 10.. = Q8 dequant (4 warps for K, 4 for V) or bf16 V
-// fix-up (1 warp).
+// Warp roles: 0 = copy producer, 1 = TMEM owner + S MMA issuer, 2..9 =
+// softmax/epilogue (two warps per TMEM lane quadrant), 13 (Q8) or 11
+// (bf16) = P.V MMA issuer, Q8: 10, 11, 12, 14 dequantise K and 15, 16,
+// 18, 19 V; bf16: 10 fixes up V tails.
 // Every wait is bounded (VA_DEV_TIMEOUT); on a timeout the CTA drains its
 // own copies and MMAs, frees TMEM and writes NaN partials.
 #include <string.h>
