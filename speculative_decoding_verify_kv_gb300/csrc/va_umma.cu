@@ -33,8 +33,9 @@
 //
 // Warp roles: 0 = copy producer, 1 = TMEM owner + S MMA issuer, 2..9 =
 // softmax/epilogue (two warps per TMEM lane quadrant), 13 (Q8) or 11
-// (bf16) = P.V MMA issuer, Q8: 10, 11, 12, 14 dequantise K and 15, 16,
-// 18, 19 V; bf16: 10 fixes up V tails.
+// (bf16) = P.V MMA issuer, Q8: 10, 11, 12, 17 dequantise K and 14, 15,
+// 16, 19 V (each group spread over the four sub-partitions); bf16: 10
+// fixes up V tails.
 // Every wait is bounded (VA_DEV_TIMEOUT); on a timeout the CTA drains its
 // own copies and MMAs, frees TMEM and writes NaN partials.
 #include <string.h>
@@ -65,10 +66,9 @@ struct UCfg {
   static constexpr int COL_Q = D + 2 * kNT;
   static constexpr int TMEM_COLS = (COL_Q + D / 2 <= 256) ? 256 : 512;
   static constexpr int DQ_WARPS = kQ8 ? 8 : 1;
-  // Q8: dequantisation on warps 10..19 minus 13 and 17, so that the MMA
-  // issuers' sub-partition (warp index = 1 mod 4) carries none of it; warp
-  // 13 issues the P.V MMAs.  bf16: warp 10 fixes up V tails, warp 11 issues
-  // the P.V MMAs.
+  // Q8: warp 13 issues the P.V MMAs and eight of warps 10..19 dequantise
+  // (dq_slot).  bf16: warp 10 fixes up V tails, warp 11 issues the P.V
+  // MMAs.
   static constexpr int PV_WARP = kQ8 ? 13 : 11;
   static constexpr int THREADS = (kQ8 ? 20 : 12) * 32;
   static constexpr int MAXREG = (65536 / THREADS) / 8 * 8 > 255 ? 255 : (65536 / THREADS) / 8 * 8;
@@ -104,6 +104,24 @@ enum {
 // block whose rows are 128 bytes apart (col in 16-bit elements, < 64).
 __device__ __forceinline__ uint32_t sw128_off(int row, int chunk16) {
   return (uint32_t)(row * 128 + ((chunk16 ^ (row & 7)) << 4));
+}
+
+// Q8 dequantisation slot of a warp (-1: none): slots 0..3 dequantise K,
+// 4..7 V.  Each group holds one warp of every sub-partition (warp index
+// mod 4) except that V doubles up on sub-partition 3, whose softmax warps
+// serve query rows 96..127 (idle when a KV head has at most 96 rows).
+__device__ __forceinline__ int dq_slot(int warp) {
+  switch (warp) {
+    case 10: return 0;
+    case 11: return 1;
+    case 12: return 2;
+    case 17: return 3;
+    case 14: return 4;
+    case 15: return 5;
+    case 16: return 6;
+    case 19: return 7;
+    default: return -1;
+  }
 }
 
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
@@ -955,16 +973,15 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     }
   } else {
     // ------------------------------------------------------------ dequant / fix-up
-    if (direct && (warp & 3) != 1) {
-      // Paged Q8: warps 10, 11, 12, 14 dequantise K tiles, 15, 16, 18, 19 V
-      // tiles, each group at its own pace (warp 13 issues the P.V MMAs, 17
-      // is idle).  Per tile: load the raw half-row from global memory, wait
+    if (direct && dq_slot(warp) >= 0) {
+      // Paged Q8: the K and V dequantisation groups (dq_slot) each convert
+      // their tensor's tiles at their own pace (warp 18 is idle, 13 issues
+      // the P.V MMAs).  Per tile: load the raw half-row from global memory, wait
       // until the tile buffer is free (the MMA that read its previous tile
       // has completed; tiles 1 and 2 also wait for Q to have left the
       // staging area), convert, store, release.
-      const int wq = warp - 10;
-      const int dq = wq - (wq > 3) - (wq > 7);  // 0..7 over warps 10,11,12,14,15,16,18,19
-      const int grp = dq >> 2;                  // 0 = K, 1 = V
+      const int dq = dq_slot(warp);
+      const int grp = dq >> 2;  // 0 = K, 1 = V
       const int gtid = (dq & 3) * 32 + lane;
       const int t = gtid & 63, hf = gtid >> 6;
       const unsigned char* src = reinterpret_cast<const unsigned char*>(grp ? p.v : p.k);
@@ -1000,13 +1017,12 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_QREADY8 + 3 * grp + jb));
       }
-    } else if (Q8 && (warp & 3) != 1) {
-      // Warps 10, 11, 12, 14 dequantise K tiles, 15, 16, 18, 19 V tiles, each
-      // group at its own pace, in place in the tile buffers (warp 13 issues
-      // the P.V MMAs, 17 is idle).
-      const int wq = warp - 10;
-      const int dq = wq - (wq > 3) - (wq > 7);  // 0..7 over warps 10,11,12,14,15,16,18,19
-      const int grp = dq >> 2;                  // 0 = K, 1 = V
+    } else if (Q8 && dq_slot(warp) >= 0) {
+      // The K and V dequantisation groups (dq_slot) each convert their
+      // tensor's tiles at their own pace, in place in the tile buffers (warp
+      // 18 is idle, 13 issues the P.V MMAs).
+      const int dq = dq_slot(warp);
+      const int grp = dq >> 2;  // 0 = K, 1 = V
       const int gtid = (dq & 3) * 32 + lane;
       // A failed wait does not leave the loop: each iteration has one named
       // barrier shared by the group's four warps, so a failing warp keeps
