@@ -35,6 +35,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
   // Launched as a programmatic dependent of the partial kernel: wait here
   // until that grid has finished and its writes are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // A programmatic dependent launched after this kernel (the next call's
+  // partial kernel) may now become resident; it waits for this grid to
+  // complete before it touches memory.
+  asm volatile("griddepcontrol.launch_dependents;");
   const long long item = blockIdx.x;
   const int grow = (int)(item / p.H), h = (int)(item % p.H);
   const int tcol = threadIdx.x % TC, grp = threadIdx.x / TC;
