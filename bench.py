@@ -501,7 +501,8 @@ def run_ours(args):
         for name, make in [("dflash-bf16 ctx4096 S8", lambda: sy.dflash_bf16(ctx=4096, num_splits=8)),
                            ("dflash-bf16 ctx8192 S8", lambda: sy.dflash_bf16(ctx=8192, num_splits=8)),
                            ("paged-d128 bf16 4x~29K S8", lambda: sy.paged_d128()),
-                           ("mixed tree+direct Q8 paged S8", lambda: sy.mixed_tree_direct())]:
+                           ("mixed tree+direct Q8 paged S8", lambda: sy.mixed_tree_direct()),
+                           ("mixed prefill-256+direct+tree Q8 paged S8", lambda: sy.mixed_prefill())]:
             c3 = make()
             b3 = Bench(c3, flags, l2)
             for i in range(3):

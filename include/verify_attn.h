@@ -71,7 +71,8 @@ typedef enum va_mode {
 #define VA_DEV_BAD_PARENT 0x1u   /* parent[j] not in [-1, j) */
 #define VA_DEV_BAD_BLOCK 0x2u    /* block_table entry outside [0, num_blocks) */
 #define VA_DEV_CTX_OVERFLOW 0x4u /* ctx + n exceeds capacity / the block table */
-#define VA_DEV_BAD_ROWS 0x8u     /* cu_rows not ascending, n > max_rows_per_seq, or total mismatch */
+#define VA_DEV_BAD_ROWS 0x8u     /* cu_rows not ascending, n > max_rows_per_seq, total mismatch,
+                                    or a tree sequence with more than VA_MAX_TREE_ROWS rows */
 #define VA_DEV_TIMEOUT 0x10u     /* a bounded pipeline wait gave up */
 
 /* Problem flags. */
@@ -125,6 +126,14 @@ typedef struct va_kv {
  *      its own sequence (lucebox PR #686, "Correctness failure found during
  *      qualification").
  */
+/* Rows per sequence: a chain sequence (a prefill segment, a draft chain or
+ * a one-row direct row; causal among its own rows) may hold up to
+ * VA_MAX_ROWS_PER_SEQ rows, a tree suffix up to VA_MAX_TREE_ROWS (its
+ * visibility is a 32-bit ancestor mask).  Rows beyond 128 / G per KV head
+ * run as further row blocks, each reading that sequence's K/V again. */
+#define VA_MAX_ROWS_PER_SEQ 1024
+#define VA_MAX_TREE_ROWS 32
+
 typedef struct va_problem {
   int32_t num_seqs;
   int32_t num_heads;
@@ -135,7 +144,8 @@ typedef struct va_problem {
   const int32_t *parent;
   const uint8_t *seq_kind;
   int32_t total_rows;          /* host copy of cu_rows[num_seqs] */
-  int32_t max_rows_per_seq;    /* host bound on rows per sequence, 1..32 */
+  int32_t max_rows_per_seq;    /* host bound on rows per sequence, 1..VA_MAX_ROWS_PER_SEQ
+                                  (VA_MODE_TREE: 1..VA_MAX_TREE_ROWS) */
   float scale;
   int32_t num_splits;
   uint32_t flags;              /* VA_FLAG_* */

@@ -26,6 +26,10 @@ DEV_CTX_OVERFLOW = 0x4
 DEV_BAD_ROWS = 0x8
 DEV_TIMEOUT = 0x10
 
+# Rows per sequence (chain / tree); see VA_MAX_ROWS_PER_SEQ in the header.
+MAX_ROWS_PER_SEQ = 1024
+MAX_TREE_ROWS = 32
+
 STATUS_NAMES = {0: "VA_OK", 1: "VA_ERR_INVALID_ARG", 2: "VA_ERR_UNSUPPORTED",
                 3: "VA_ERR_ALIGNMENT", 4: "VA_ERR_WORKSPACE_TOO_SMALL", 5: "VA_ERR_CUDA"}
 

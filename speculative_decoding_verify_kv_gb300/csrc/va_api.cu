@@ -71,7 +71,8 @@ static va_status check(const va_problem* p, const va_kv* kv, int mode) {
   int G = p->num_heads / kv->num_kv_heads;
   if (G > 8) return VA_ERR_UNSUPPORTED;
   if (kv->head_dim != 64 && kv->head_dim != 128 && kv->head_dim != 256) return VA_ERR_UNSUPPORTED;
-  if (p->max_rows_per_seq > 32) return VA_ERR_UNSUPPORTED;
+  if (p->max_rows_per_seq > kMaxRows) return VA_ERR_UNSUPPORTED;
+  if (mode == VA_MODE_TREE && p->max_rows_per_seq > kMaxTreeRows) return VA_ERR_UNSUPPORTED;
   if (p->num_splits > 256) return VA_ERR_UNSUPPORTED;
   if (p->q_dtype == VA_Q8_0) return VA_ERR_UNSUPPORTED;
   if (kv->dtype != VA_F32 && p->q_dtype != VA_BF16) return VA_ERR_UNSUPPORTED;
@@ -345,8 +346,9 @@ va_status va_debug_row_map(const va_problem* p, int32_t mode, int32_t* row_seq,
                            uint32_t* anc_mask, uint32_t* status, void* stream) {
   if (!p || !p->cu_rows || !p->ctx_len) return VA_ERR_INVALID_ARG;
   if (mode < VA_MODE_CHAIN || mode > VA_MODE_MIXED) return VA_ERR_INVALID_ARG;
-  if (p->num_seqs < 1 || p->max_rows_per_seq < 1 || p->max_rows_per_seq > 32)
+  if (p->num_seqs < 1 || p->max_rows_per_seq < 1 || p->max_rows_per_seq > kMaxRows)
     return VA_ERR_INVALID_ARG;
+  if (mode == VA_MODE_TREE && p->max_rows_per_seq > kMaxTreeRows) return VA_ERR_INVALID_ARG;
   if (mode != VA_MODE_CHAIN && !p->parent) return VA_ERR_INVALID_ARG;
   if (mode == VA_MODE_MIXED && !p->seq_kind) return VA_ERR_INVALID_ARG;
   if (p->total_rows == 0) return VA_OK;

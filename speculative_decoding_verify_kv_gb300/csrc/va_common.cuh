@@ -87,8 +87,15 @@ __device__ __forceinline__ int seq_kind_of(const Params& p, int s) {
   return p.seq_kind[s] ? 1 : 0;
 }
 
+// Rows per sequence: chain sequences (prefill segments, draft chains and
+// one-row direct rows) up to kMaxRows, tree suffixes up to kMaxTreeRows
+// (their visibility is a 32-bit ancestor mask).
+constexpr int kMaxRows = VA_MAX_ROWS_PER_SEQ;
+constexpr int kMaxTreeRows = VA_MAX_TREE_ROWS;
+
 // Ancestor mask of local row j: bit a set iff draft position a is visible
-// to row j (a == j or a is an ancestor).  The walk strictly decreases, so it
+// to row j (a == j or a is an ancestor).  A chain row j >= 31 gets every
+// bit (draft_visible decides chain visibility from j itself).  The walk strictly decreases, so it
 // ends within j steps; a parent outside [-1, current) flags an error.
 __device__ __forceinline__ unsigned row_mask(int kind, const int* parent_seq, int j,
                                              bool* bad) {
@@ -106,6 +113,12 @@ __device__ __forceinline__ unsigned row_mask(int kind, const int* parent_seq, in
     par = parent_seq[cur];
   }
   return m;
+}
+
+// Is draft position a (0 <= a < n) visible to local row j?  Chain: a <= j
+// (causal).  Tree: bit a of the row's ancestor mask (n <= kMaxTreeRows).
+__device__ __forceinline__ bool draft_visible(int kind, unsigned anc, int j, int a) {
+  return kind == 0 ? a <= j : ((anc >> a) & 1u) != 0u;
 }
 
 // Row of token t of (sequence s, KV head kvh), counted in rows of the k/v
@@ -128,6 +141,7 @@ __device__ __forceinline__ unsigned check_sequence(const Params& p, int s, int* 
   *ctx = c;
   unsigned err = 0;
   if (r1 < r0 || r1 - r0 > p.max_rows || r0 < 0 || r1 > p.total_rows) err |= VA_DEV_BAD_ROWS;
+  else if (r1 - r0 > kMaxTreeRows && seq_kind_of(p, s) == 1) err |= VA_DEV_BAD_ROWS;
   if (c < 0) err |= VA_DEV_CTX_OVERFLOW;
   if (!err) {
     long long L = (long long)c + (r1 - r0);

@@ -5,22 +5,22 @@
 
 namespace va {
 
-// One thread per (sequence, local row slot up to max_rows).
+// One block per sequence, its threads striding over the local rows.
 __global__ void debug_row_map_kernel(const Params p, int* row_seq, unsigned* anc) {
   const int s = blockIdx.x;
-  const int j = threadIdx.x;
   int row0, n, ctx;
   unsigned err = check_sequence(p, s, &row0, &n, &ctx);
   if (err & VA_DEV_BAD_ROWS) {
-    if (j == 0) flag(p.status, err & VA_DEV_BAD_ROWS);
+    if (threadIdx.x == 0) flag(p.status, err & VA_DEV_BAD_ROWS);
     return;
   }
-  if (j >= n) return;
-  bool bad = false;
-  unsigned m = row_mask(seq_kind_of(p, s), p.parent + row0, j, &bad);
-  if (bad) flag(p.status, VA_DEV_BAD_PARENT);
-  row_seq[row0 + j] = s;
-  anc[row0 + j] = m;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    bool bad = false;
+    unsigned m = row_mask(seq_kind_of(p, s), p.parent + row0, j, &bad);
+    if (bad) flag(p.status, VA_DEV_BAD_PARENT);
+    row_seq[row0 + j] = s;
+    anc[row0 + j] = m;
+  }
 }
 
 // One thread per (sequence, token < max_len).

@@ -133,7 +133,8 @@ __global__ void __launch_bounds__(kSimtThreads) simt_partial_kernel(const Params
         float dot = 0.f;
 #pragma unroll 8
         for (int d = 0; d < D; ++d) dot = fmaf(Qs[rl * D + d], Ks[lane * (D + 1) + d], dot);
-        bool vis = tok < shi && (tok < ctx || ((mask_s[rl] >> (tok - ctx)) & 1u));
+        bool vis = tok < shi &&
+                   (tok < ctx || draft_visible(kind, mask_s[rl], (rbase + rl) / p.G, tok - ctx));
         float s2 = vis ? dot * p.scale_log2 : -INFINITY;
         float mt = s2;
 #pragma unroll

@@ -862,7 +862,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const int t = t0 + c;
-            const bool vis = rvalid && t < shi && (t < ctx || ((anc >> (t - ctx)) & 1u));
+            const bool vis = rvalid && t < shi && (t < ctx || draft_visible(kind, anc, j, t - ctx));
             sv[c] = vis ? __uint_as_float(sr[c]) : -INFINITY;
             mx = fmaxf(mx, sv[c]);
           }

@@ -373,6 +373,18 @@ def mixed_tree_direct(num_splits: int = 8, seed: int = 1005, ctx=None,
                      num_splits=num_splits)
 
 
+def mixed_prefill(num_splits: int = 8, seed: int = 1006, ctx=(8192, 16383, 20676, 4097, 32768),
+                  rows=(256, 1, 1, 8, 8), kinds=(0, 0, 0, 1, 1)) -> VerifyCase:
+    """A mixed launch with a prefill segment: sequence 0 is a 256-row chain
+    (causal among its own rows, more rows than a tree's 32-bit ancestor
+    mask holds), two sequences contribute one direct row and two a width-8
+    seeded random tree suffix.  H24/KV4/D256 over paged Q8_0."""
+    return make_case("mixed-prefill-q8", num_heads=24, num_kv_heads=4, head_dim=256,
+                     kv_dtype=Q8_0, q_dtype=BF16, ctx=list(ctx), rows=list(rows),
+                     kinds=list(kinds), mode="mixed", paged=True, seed=seed,
+                     num_splits=num_splits)
+
+
 def subset_sequences(case: VerifyCase, seqs) -> VerifyCase:
     """A launch holding only the given sequences (same cache/pool, same
     values): used for the launch-composition invariance check."""

@@ -294,6 +294,11 @@ def brute_cases():
                      kinds=[1, 0, 1], mode="mixed", paged=True, seed=23, extra_blocks=2),
         sy.make_case("bf-q8-chain", num_heads=6, num_kv_heads=3, head_dim=64, kv_dtype=sy.Q8_0,
                      q_dtype=sy.F32, ctx=[20], rows=[2], seed=24),
+        # A 40-row chain (a prefill segment: more rows than a 32-bit
+        # ancestor mask holds) beside a tree suffix in one mixed launch.
+        sy.make_case("bf-f32-prefill-mixed", num_heads=2, num_kv_heads=1, head_dim=8,
+                     kv_dtype=sy.F32, q_dtype=sy.F32, ctx=[3, 6], rows=[40, 5], kinds=[0, 1],
+                     mode="mixed", seed=25),
     ]
 
 

@@ -90,7 +90,7 @@ def test_validate_ok():
     (dict(kv=dict(k=None)), 1), (dict(kv=dict(dtype=9)), 1), (dict(kv=dict(capacity=0)), 1),
     (dict(kv=dict(page_size=16, block_table=None, max_blocks_per_seq=4, num_blocks=4)), 1),
     (dict(p=dict(num_heads=25)), 2), (dict(kv=dict(head_dim=96)), 2),
-    (dict(p=dict(max_rows_per_seq=33)), 2), (dict(kv=dict(page_size=32)), 2),
+    (dict(p=dict(max_rows_per_seq=1025)), 2), (dict(kv=dict(page_size=32)), 2),
     (dict(kv=dict(capacity=100)), 2), (dict(p=dict(num_heads=72)), 2),
     (dict(p=dict(q_dtype=va.F32)), 2), (dict(p=dict(num_splits=1000)), 2),
     (dict(kv=dict(k=FAKE + 8)), 3), (dict(kv=dict(v=FAKE + 2)), 3), (dict(p=dict(q=FAKE + 4)), 3),
@@ -99,6 +99,21 @@ def test_validate_rejects(bad, code):
     p = _problem(**bad.get("p", {}))
     kv = _kv(**bad.get("kv", {}))
     assert validate(p, kv) == code
+
+
+def test_row_limits_by_sequence_kind():
+    # Chain sequences (prefill segments, draft chains) take up to 1024 rows;
+    # a tree launch is limited to 32 rows per sequence (the ancestor mask);
+    # a mixed launch defers the tree limit to the device (VA_DEV_BAD_ROWS).
+    assert va.MAX_ROWS_PER_SEQ == 1024 and va.MAX_TREE_ROWS == 32
+    text = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                             "include", "verify_attn.h")).read()
+    assert "#define VA_MAX_ROWS_PER_SEQ 1024" in text and "#define VA_MAX_TREE_ROWS 32" in text
+    for mode in (va.MODE_CHAIN, va.MODE_MIXED):
+        assert validate(_problem(max_rows_per_seq=1024), _kv(), mode) == 0
+        assert validate(_problem(max_rows_per_seq=1025), _kv(), mode) == 2
+    assert validate(_problem(max_rows_per_seq=32), _kv(), va.MODE_TREE) == 0
+    assert validate(_problem(max_rows_per_seq=33), _kv(), va.MODE_TREE) == 2
 
 
 def test_tree_and_mixed_need_metadata():
