@@ -87,7 +87,17 @@ typedef enum va_mode {
  *     slot t%16 (lucebox PR #686, "Correctness failure found during
  *     qualification": 16-token blocks).
  *   row = head_dim fp32 / bf16 elements, or head_dim/32 Q8_0 blocks of 34 bytes.
- *   The draft rows' own K/V sit at positions ctx .. ctx+n-1 of the same cache.
+ *   The draft rows' own K/V sit at positions ctx .. ctx+n-1 of the same cache,
+ *   except for tree sequences when a tree scratch KV is given (draft_k,
+ *   draft_v: device [total_rows][num_kv_heads][row], row r of the launch in
+ *   the cache's row format, 16-byte aligned).  Then a tree sequence's draft
+ *   position a reads scratch row cu_rows[s] + a, and its cache needs room
+ *   for the context only (capacity, or block-table entries, for ctx_len[s]
+ *   tokens).  Chain and direct sequences always read the cache: prefill and
+ *   direct rows write durable KV, tree rows write scratch KV (lucebox PR
+ *   #686, "State and commit invariants").  With a scratch KV the
+ *   tensor-core kernel serves Q8_0 paged caches; other caches run on the
+ *   CUDA-core kernel.
  */
 typedef struct va_kv {
   va_dtype dtype;
@@ -100,6 +110,8 @@ typedef struct va_kv {
   const int32_t *block_table;  /* paged only: device [num_seqs][max_blocks_per_seq] */
   int32_t max_blocks_per_seq;  /* paged only */
   int32_t num_blocks;          /* paged only: blocks in the pool */
+  const void *draft_k;         /* optional tree scratch KV (see above), or NULL */
+  const void *draft_v;         /* set together with draft_k */
 } va_kv;
 
 /*
@@ -153,6 +165,31 @@ typedef struct va_problem {
 
 /* Library version (major*10000 + minor*100 + patch). */
 int32_t va_version(void);
+
+/*
+ * Tree commit of the KV cache (the KV part of lucebox PR #686's tree commit
+ * transaction, "State and commit invariants": tree rows write scratch KV;
+ * the commit promotes only the accepted prefix and checks every domain
+ * before it mutates any).  For each sequence s, the accepted path of m_s =
+ * accepted_len[s] tree nodes, accepted_nodes[cu_rows[s] + i] for i < m_s
+ * (root first), goes from the tree scratch KV (kv->draft_k / draft_v, row
+ * cu_rows[s] + node) to positions ctx_len[s] + i of the cache, K and V of
+ * every KV head, byte for byte.  accepted_len: device [num_seqs];
+ * accepted_nodes: device [total_rows] (entries past m_s ignored).
+ * Device preflight before any write, for every sequence: the row checks of
+ * a verify call (VA_DEV_BAD_ROWS, VA_DEV_CTX_OVERFLOW on the context);
+ * 0 <= m <= n and m = 0 unless the sequence is a tree (VA_DEV_BAD_ROWS);
+ * nodes in [0, n) (VA_DEV_BAD_ROWS) forming a root path: parent[first] =
+ * -1, parent[next] = previous (VA_DEV_BAD_PARENT); positions up to
+ * ctx + m within capacity or the block table (VA_DEV_CTX_OVERFLOW) on
+ * valid blocks (VA_DEV_BAD_BLOCK).  If the status word holds any bit after
+ * the preflight, nothing is written: *status must be 0 on entry.  Host
+ * checks as for the verify calls; kv->draft_k, accepted_len and status are
+ * required (VA_ERR_INVALID_ARG).  The scratch must not overlap the cache.
+ */
+va_status verify_attn_promote(const va_problem *p, const va_kv *kv, int32_t mode,
+                              const int32_t *accepted_len, const int32_t *accepted_nodes,
+                              uint32_t *status, void *stream);
 
 /* Human-readable name of a status code; never NULL. */
 const char *va_status_string(va_status s);

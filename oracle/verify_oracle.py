@@ -36,6 +36,13 @@ sequence's own span L and the split count S, never on what else shares the
 launch (lucebox PR #686, section "Correctness failure found during
 qualification": the 1,024-token partition boundary).
 
+Optional tree scratch KV and the tree commit (lucebox PR #686, "State and
+commit invariants": tree rows write scratch KV; the commit transaction
+promotes only the accepted prefix after checking every domain): with
+``draft_k``/``draft_v`` a tree sequence's draft position a reads scratch row
+``cu_rows[s] + a``; ``promote`` copies each tree's accepted root path to
+positions ``ctx ..`` of the cache, or nothing at all if any check fails.
+
 Parity status: every function below is pinned by ``tests/test_oracle.py``
 (brute force, closed forms, library special cases, invariants and hand-worked
 fixtures under ``tests/golden/``).
@@ -246,17 +253,35 @@ def merge(parts):
 # ---------------------------------------------------------------------------
 # The whole verify launch.
 
+def span_rows(cache, draft, s: int, kvh: int, ctx: int, n: int, lo: int, *, page_size: int,
+              capacity: int, num_kv_heads: int, block_table=None) -> np.ndarray:
+    """Storage rows of the span's L = ctx + n tokens for (s, kvh): all from
+    the cache, or (``draft`` given: a tree scratch KV [total_rows][KVH][row])
+    the ctx context rows from the cache followed by scratch rows lo .. lo+n-1
+    for the draft positions (lucebox PR #686, "State and commit invariants":
+    tree rows write scratch KV)."""
+    if draft is None:
+        return kv_rows(cache, s, kvh, ctx + n, page_size=page_size, capacity=capacity,
+                       num_kv_heads=num_kv_heads, block_table=block_table)
+    ctx_part = kv_rows(cache, s, kvh, ctx, page_size=page_size, capacity=capacity,
+                       num_kv_heads=num_kv_heads, block_table=block_table)
+    return np.concatenate([ctx_part, np.asarray(draft)[lo:lo + n, kvh]])
+
+
 def verify_attention(q, k, v, *, kv_dtype: str, q_dtype: str, num_heads: int,
                      num_kv_heads: int, head_dim: int, ctx_len, cu_rows,
                      parent=None, seq_kind=None, mode: str = "chain",
                      page_size: int = 0, capacity: int = 0, block_table=None,
+                     draft_k=None, draft_v=None,
                      scale: float = 0.0, num_splits: Optional[int] = None,
                      rows: Optional[list] = None, heads: Optional[list] = None,
                      return_weights: bool = False):
     """Verify attention for every (row, head) (or the ``rows`` x ``heads``
     subset).  Returns O [total_rows, H, D] and LSE [total_rows, H] in float64
     (entries outside the subset are NaN).  ``num_splits=None`` is the
-    unsplit definition; an integer S takes the split-and-merge route."""
+    unsplit definition; an integer S takes the split-and-merge route.
+    ``draft_k``/``draft_v`` (optional tree scratch KV): a tree sequence's
+    draft K/V come from scratch rows cu_rows[s] + a instead of the cache."""
     H, KVH, D = num_heads, num_kv_heads, head_dim
     if H % KVH:
         raise ValueError("H must be a multiple of KVH")
@@ -282,11 +307,14 @@ def verify_attention(q, k, v, *, kv_dtype: str, q_dtype: str, num_heads: int,
         L = ctx + n
         kind = seq_kind_of(s, seq_kind, mode)
         pl = None if parent is None else np.asarray(parent)[lo:hi]
+        scratch = draft_k is not None and kind == 1
         for kvh in sorted(set(kv_head_of(h, G) for h in headset)):
-            K = decode_rows(kv_rows(k, s, kvh, L, page_size=page_size, capacity=capacity,
-                                    num_kv_heads=KVH, block_table=block_table), kv_dtype)
-            V = decode_rows(kv_rows(v, s, kvh, L, page_size=page_size, capacity=capacity,
-                                    num_kv_heads=KVH, block_table=block_table), kv_dtype)
+            K = decode_rows(span_rows(k, draft_k if scratch else None, s, kvh, ctx, n, lo,
+                                      page_size=page_size, capacity=capacity,
+                                      num_kv_heads=KVH, block_table=block_table), kv_dtype)
+            V = decode_rows(span_rows(v, draft_v if scratch else None, s, kvh, ctx, n, lo,
+                                      page_size=page_size, capacity=capacity,
+                                      num_kv_heads=KVH, block_table=block_table), kv_dtype)
             for r in todo:
                 j = r - lo
                 pos = visible_positions(ctx, n, kind, pl, j)
@@ -318,4 +346,79 @@ def verify_case(case, **kw):
         head_dim=case.head_dim, ctx_len=case.ctx_len, cu_rows=case.cu_rows,
         parent=case.parent, seq_kind=case.seq_kind, mode=case.mode,
         page_size=case.page_size, capacity=case.capacity,
-        block_table=case.block_table, scale=case.scale, **kw)
+        block_table=case.block_table, draft_k=getattr(case, "draft_k", None),
+        draft_v=getattr(case, "draft_v", None), scale=case.scale, **kw)
+
+
+# ---------------------------------------------------------------------------
+# Tree commit of the KV (the KV part of lucebox PR #686's tree commit
+# transaction, "State and commit invariants": only the accepted prefix is
+# promoted, and every domain is checked before any is mutated).
+
+def promote_preflight(*, ctx_len, cu_rows, parent, seq_kind, mode: str, accepted_len,
+                      accepted_nodes, page_size: int, capacity: int, num_blocks: int = 0,
+                      block_table=None) -> set:
+    """The reasons the commit must not happen (empty set: it may).  Per
+    sequence: m in [0, n], m > 0 only for a tree; the accepted nodes are a
+    root path of the tree (first node's parent -1, each next node's parent
+    the previous node); the destinations ctx .. ctx+m-1 fit the capacity
+    or the block table, on valid blocks."""
+    bad = set()
+    cu = np.asarray(cu_rows)
+    for s in range(len(cu) - 1):
+        lo, hi = int(cu[s]), int(cu[s + 1])
+        n, m, ctx = hi - lo, int(accepted_len[s]), int(ctx_len[s])
+        if m < 0 or m > n or (m > 0 and seq_kind_of(s, seq_kind, mode) != 1):
+            bad.add("rows")
+            continue
+        path = [int(a) for a in accepted_nodes[lo:lo + m]]
+        if any(a < 0 or a >= n for a in path):
+            bad.add("rows")
+            continue
+        expected_parent = [-1] + path[:-1]
+        if any(int(parent[lo + a]) != e for a, e in zip(path, expected_parent)):
+            bad.add("parent")
+            continue
+        end = ctx + m
+        if page_size == 0:
+            if end > capacity:
+                bad.add("overflow")
+        else:
+            pages = -(-end // PAGE)
+            bt = np.asarray(block_table)
+            if pages > bt.shape[1]:
+                bad.add("overflow")
+            elif any(not (0 <= int(bt[s, pg]) < num_blocks) for pg in range(ctx // PAGE, pages)):
+                bad.add("block")
+    return bad
+
+
+def promote(k, v, draft_k, draft_v, *, ctx_len, cu_rows, parent, seq_kind, mode: str,
+            accepted_len, accepted_nodes, page_size: int, capacity: int, num_kv_heads: int,
+            block_table=None):
+    """Cache arrays after the commit (copies; the inputs are not changed):
+    path node i of sequence s (scratch row cu_rows[s] + node) lands at
+    position ctx + i, every KV head, K and V.  Returns (k', v', reasons);
+    any reason leaves both caches exactly as they were."""
+    nb = 0 if page_size == 0 else np.asarray(k).shape[0]
+    bad = promote_preflight(ctx_len=ctx_len, cu_rows=cu_rows, parent=parent,
+                            seq_kind=seq_kind, mode=mode, accepted_len=accepted_len,
+                            accepted_nodes=accepted_nodes, page_size=page_size,
+                            capacity=capacity, num_blocks=nb, block_table=block_table)
+    k2, v2 = np.array(k, copy=True), np.array(v, copy=True)
+    if bad:
+        return k2, v2, bad
+    kf = k2.reshape(-1, k2.shape[-1])
+    vf = v2.reshape(-1, v2.shape[-1])
+    cu = np.asarray(cu_rows)
+    for s in range(len(cu) - 1):
+        lo = int(cu[s])
+        ctx = int(ctx_len[s])
+        for i in range(int(accepted_len[s])):
+            a = int(accepted_nodes[lo + i])
+            for kvh in range(num_kv_heads):
+                dst = int(gather_index(s, kvh, ctx + i, page_size=page_size, capacity=capacity,
+                                       num_kv_heads=num_kv_heads, block_table=block_table))
+                kf[dst] = np.asarray(draft_k)[lo + a, kvh]
+                vf[dst] = np.asarray(draft_v)[lo + a, kvh]
+    return k2, v2, bad

@@ -39,7 +39,7 @@ MODE_CODES = {"chain": MODE_CHAIN, "tree": MODE_TREE, "mixed": MODE_MIXED}
 EXPORTED = ["va_version", "va_status_string", "va_last_cuda_error", "va_workspace_size", "va_validate",
             "verify_attn_chain", "verify_attn_tree", "verify_attn_mixed",
             "va_debug_row_map", "va_debug_gather_index", "va_plan", "va_timing_enable",
-            "va_timing_read", "verify_attn_noalloc"]
+            "va_timing_read", "verify_attn_noalloc", "verify_attn_promote"]
 
 
 class VaKV(ctypes.Structure):
@@ -47,7 +47,8 @@ class VaKV(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
                 ("page_size", ctypes.c_int32), ("capacity", ctypes.c_int64),
                 ("block_table", ctypes.c_void_p), ("max_blocks_per_seq", ctypes.c_int32),
-                ("num_blocks", ctypes.c_int32)]
+                ("num_blocks", ctypes.c_int32), ("draft_k", ctypes.c_void_p),
+                ("draft_v", ctypes.c_void_p)]
 
 
 class VaProblem(ctypes.Structure):
@@ -104,6 +105,9 @@ def _load():
     lib.va_timing_read.restype = ctypes.c_int
     lib.va_timing_read.argtypes = [ctypes.c_int32, P(ctypes.c_float), P(ctypes.c_float),
                                    P(ctypes.c_int32)]
+    lib.verify_attn_promote.restype = ctypes.c_int
+    lib.verify_attn_promote.argtypes = [P(VaProblem), P(VaKV), ctypes.c_int32, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     return lib
 
 
@@ -146,11 +150,14 @@ class KV:
     block_table: object = None
     max_blocks_per_seq: int = 0
     num_blocks: int = 0
+    draft_k: object = None  # optional tree scratch KV [total_rows][KVH][row]
+    draft_v: object = None
 
     def c(self) -> VaKV:
         return VaKV(self.dtype, self.num_kv_heads, self.head_dim, _ptr(self.k), _ptr(self.v),
                     self.page_size, self.capacity, _ptr(self.block_table),
-                    self.max_blocks_per_seq, self.num_blocks)
+                    self.max_blocks_per_seq, self.num_blocks, _ptr(self.draft_k),
+                    _ptr(self.draft_v))
 
 
 @dataclass
@@ -256,6 +263,21 @@ def verify_attn_noalloc(p: Problem, kv: KV, mode: int, o, lse, status=None, stre
     return o, lse
 
 
+def verify_attn_promote(p: Problem, kv: KV, mode: int, accepted_len, accepted_nodes, status,
+                        stream=None):
+    """Copy each tree sequence's accepted path from the tree scratch KV
+    (``kv.draft_k/draft_v``) into the cache at positions ctx..ctx+m-1, as
+    one device-checked transaction (nothing is written if the preflight
+    flags any sequence).  ``accepted_len`` int32 [num_seqs] and
+    ``accepted_nodes`` int32 [total_rows] are device tensors; ``status`` is a
+    zeroed device int32 word that receives the VA_DEV_* bits."""
+    st = lib.verify_attn_promote(ctypes.byref(p.c()), ctypes.byref(kv.c()), mode,
+                                 _ptr(accepted_len), _ptr(accepted_nodes), _ptr(status),
+                                 _stream_handle(stream))
+    if st:
+        raise VaError(st, "verify_attn_promote")
+
+
 def debug_row_map(p: Problem, mode: int, status=None, stream=None):
     import torch
     dev = p.cu_rows.device
@@ -295,10 +317,14 @@ def upload(case, device="cuda", num_splits=None, flags: int = 0):
     k = dev(case.k.view(np.int16) if case.k.dtype == np.uint16 else case.k)
     v = dev(case.v.view(np.int16) if case.v.dtype == np.uint16 else case.v)
     bt = None if case.block_table is None else dev(case.block_table.astype(np.int32))
+    dk = getattr(case, "draft_k", None)
+    dv = getattr(case, "draft_v", None)
     kv = KV(DTYPE_CODES[case.kv_dtype], case.num_kv_heads, case.head_dim, k, v,
             page_size=case.page_size, capacity=case.capacity, block_table=bt,
             max_blocks_per_seq=0 if bt is None else int(case.block_table.shape[1]),
-            num_blocks=0 if bt is None else int(case.k.shape[0]))
+            num_blocks=0 if bt is None else int(case.k.shape[0]),
+            draft_k=None if dk is None else dev(dk.view(np.int16) if dk.dtype == np.uint16 else dk),
+            draft_v=None if dv is None else dev(dv.view(np.int16) if dv.dtype == np.uint16 else dv))
     p = Problem(num_seqs=case.num_seqs, num_heads=case.num_heads,
                 q_dtype=DTYPE_CODES[case.q_dtype], q=q,
                 cu_rows=dev(case.cu_rows.astype(np.int32)),

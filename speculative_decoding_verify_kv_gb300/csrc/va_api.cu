@@ -29,6 +29,8 @@ static va_status note_cuda(cudaError_t e) {
 }
 cudaError_t launch_merge(const Params& p, cudaStream_t st);
 cudaError_t launch_debug_row_map(const Params& p, int* row_seq, unsigned* anc, cudaStream_t st);
+cudaError_t launch_promote(const Params& p, const int* acc_len, const int* nodes,
+                           cudaStream_t st);
 cudaError_t launch_debug_gather(const Params& p, int kvh, long long max_len, long long* out,
                                 cudaStream_t st);
 
@@ -83,6 +85,8 @@ static va_status check(const va_problem* p, const va_kv* kv, int mode) {
   if (mode != VA_MODE_CHAIN && !p->parent) return VA_ERR_INVALID_ARG;
   if (mode == VA_MODE_MIXED && !p->seq_kind) return VA_ERR_INVALID_ARG;
   if (!kv->k || !kv->v) return VA_ERR_INVALID_ARG;
+  if (!kv->draft_k != !kv->draft_v) return VA_ERR_INVALID_ARG;
+  if (kv->draft_k && (!aligned16(kv->draft_k) || !aligned16(kv->draft_v))) return VA_ERR_ALIGNMENT;
   if (kv->page_size == 0) {
     if (kv->capacity < 1) return VA_ERR_INVALID_ARG;
     if (kv->capacity % kPage) return VA_ERR_UNSUPPORTED;
@@ -107,7 +111,10 @@ static Plan make_plan(const va_problem* p, const va_kv* kv) {
   Plan pl;
   const int G = p->num_heads / kv->num_kv_heads;
   // Kernel choice from the cache dtype and the caller's flag only.
-  const bool tensor = kv->dtype != VA_F32 && !(p->flags & VA_FLAG_CUDA_CORES);
+  // With a tree scratch KV the tensor-core kernel serves Q8_0 paged caches
+  // (its dequantising warps load each row through its own address).
+  const bool scratch_ok = !kv->draft_k || (kv->dtype == VA_Q8_0 && kv->page_size == kPage);
+  const bool tensor = kv->dtype != VA_F32 && !(p->flags & VA_FLAG_CUDA_CORES) && scratch_ok;
   pl.kernel = tensor ? 1 : 0;
   pl.rows_per_block = tensor ? kUmmaRowsPerBlock : kSimtRowsPerBlock;
   pl.threads = tensor ? umma_threads(kv->head_dim, kv->dtype) : kSimtThreadsPerBlock;
@@ -167,6 +174,8 @@ static Params make_params(const va_problem* p, const va_kv* kv, int mode, const 
   q.seq_kind = p->seq_kind;
   q.k = kv->k;
   q.v = kv->v;
+  q.dk = kv->draft_k;
+  q.dv = kv->draft_v;
   q.page_size = kv->page_size;
   q.capacity = kv->capacity;
   q.block_table = kv->block_table;
@@ -380,6 +389,19 @@ va_status va_debug_gather_index(const va_problem* p, const va_kv* kv, int32_t kv
   Params q = make_params(p, kv, VA_MODE_CHAIN, pl, nullptr, nullptr, nullptr, status);
   cudaError_t e = launch_debug_gather(q, kv_head, (long long)max_len, (long long*)phys_row,
                                       (cudaStream_t)stream);
+  return e == cudaSuccess ? VA_OK : note_cuda(e);
+}
+
+va_status verify_attn_promote(const va_problem* p, const va_kv* kv, int32_t mode,
+                              const int32_t* accepted_len, const int32_t* accepted_nodes,
+                              uint32_t* status, void* stream) {
+  va_status st = check(p, kv, mode);
+  if (st != VA_OK) return st;
+  if (!kv->draft_k || !accepted_len || !status) return VA_ERR_INVALID_ARG;
+  if (p->total_rows > 0 && !accepted_nodes) return VA_ERR_INVALID_ARG;
+  Plan pl = make_plan(p, kv);
+  Params q = make_params(p, kv, mode, pl, nullptr, nullptr, nullptr, status);
+  cudaError_t e = launch_promote(q, accepted_len, accepted_nodes, (cudaStream_t)stream);
   return e == cudaSuccess ? VA_OK : note_cuda(e);
 }
 

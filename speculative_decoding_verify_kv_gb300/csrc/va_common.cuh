@@ -34,6 +34,8 @@ struct Params {
   const unsigned char* seq_kind;
   const void* k;
   const void* v;
+  const void* dk;         // tree scratch KV [total_rows][KVH][row], or null
+  const void* dv;
   int page_size;
   long long capacity;
   const int* block_table;
@@ -130,8 +132,20 @@ __device__ __forceinline__ long long kv_row(const Params& p, int s, int kvh, int
   return ((long long)blk * p.KVH + kvh) * kPage + (t % kPage);
 }
 
+// Does sequence s (of the given kind) read its draft K/V from the tree
+// scratch KV (row cu_rows[s] + a for draft position a)?
+__device__ __forceinline__ bool uses_scratch(const Params& p, int kind) {
+  return p.dk != nullptr && kind == 1;
+}
+
+// Scratch row (counted in rows of dk / dv) of draft position a.
+__device__ __forceinline__ long long scratch_row(const Params& p, int row0, int kvh, int a) {
+  return (long long)(row0 + a) * p.KVH + kvh;
+}
+
 // Validate sequence s: row count and the span against capacity / the block
-// table.  Returns the error bits (0 if fine).
+// table (the context only when its drafts sit in the scratch KV).  Returns
+// the error bits (0 if fine).
 __device__ __forceinline__ unsigned check_sequence(const Params& p, int s, int* row0, int* n,
                                                    int* ctx) {
   int r0 = p.cu_rows[s], r1 = p.cu_rows[s + 1];
@@ -144,7 +158,7 @@ __device__ __forceinline__ unsigned check_sequence(const Params& p, int s, int* 
   else if (r1 - r0 > kMaxTreeRows && seq_kind_of(p, s) == 1) err |= VA_DEV_BAD_ROWS;
   if (c < 0) err |= VA_DEV_CTX_OVERFLOW;
   if (!err) {
-    long long L = (long long)c + (r1 - r0);
+    long long L = (long long)c + (uses_scratch(p, seq_kind_of(p, s)) ? 0 : r1 - r0);
     if (p.page_size == 0) {
       if (L > p.capacity) err |= VA_DEV_CTX_OVERFLOW;
     } else {

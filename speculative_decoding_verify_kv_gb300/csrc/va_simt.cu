@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_partial_kernel(const Params
   const int nrows = min(kSimtRows, R - rbase);
   const int L = ctx + n;
   const int kind = seq_kind_of(p, s);
+  const bool scratch = uses_scratch(p, kind);  // drafts from the tree scratch KV
 
   if (tid == 0) bad_s = 0;
   __syncthreads();
@@ -107,7 +108,11 @@ __global__ void __launch_bounds__(kSimtThreads) simt_partial_kernel(const Params
         int t = i / D, d = i % D;
         int tok = t0 + t;
         float kx = 0.f, vx = 0.f;
-        if (tok < shi) {
+        if (tok < shi && tok >= ctx && scratch) {
+          const long long row = scratch_row(p, row0, kvh, tok - ctx);
+          kx = load_kv<KVT>(p.dk, row, p.row_bytes, d);
+          vx = load_kv<KVT>(p.dv, row, p.row_bytes, d);
+        } else if (tok < shi) {
           long long row = kv_row(p, s, kvh, tok);
           if (row < 0) {
             atomicOr(&bad_s, 2);

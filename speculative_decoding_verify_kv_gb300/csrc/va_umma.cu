@@ -407,6 +407,11 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
   const int j = rvalid ? rseq / G : 0;
   const int g = rvalid ? rseq % G : 0;
   const int kind = seq_kind_of(p, s);
+  // Tree sequence with a tree scratch KV: draft positions (>= ctx) are read
+  // from the scratch rows, and the cache (block table) covers the context
+  // only.  (Paged Q8 instantiation; the host routes other caches with a
+  // scratch KV to the CUDA-core kernel.)
+  const bool scratch = PAGED && uses_scratch(p, kind);
 
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -428,7 +433,8 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       const long long rowp = ((long long)s * p.KVH + kvh) * p.capacity + tp;
       bulk_prefetch_l2(src + rowp * C::RB, (uint32_t)(np * C::RB));
     } else {
-      for (int pg = 0; pg < np / kPage; ++pg) {
+      const int ncache = (scratch ? min(np, ctx - tp) : np);  // tokens in the cache
+      for (int pg = 0; pg * kPage < ncache; ++pg) {
         const int blk = p.block_table[(long long)s * p.max_blocks + tp / kPage + pg];
         bulk_prefetch_l2(src + ((long long)blk * p.KVH + kvh) * kPage * C::RB, kPage * C::RB);
       }
@@ -541,7 +547,8 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     if (bad) atomicOr(&err_s, (int)VA_DEV_BAD_PARENT);
   }
   if (!err && p.page_size != 0 && ntiles > 0) {
-    const int pg0 = slo / kPage, pg1 = (shi + kPage - 1) / kPage;
+    const int cend = scratch ? min(shi, ctx) : shi;  // cache tokens of the range
+    const int pg0 = slo / kPage, pg1 = (cend + kPage - 1) / kPage;
     for (int pg = pg0 + tid; pg < pg1; pg += blockDim.x) {
       int blk = p.block_table[(long long)s * p.max_blocks + pg];
       if (blk < 0 || blk >= p.num_blocks) atomicOr(&err_s, (int)VA_DEV_BAD_BLOCK);
@@ -985,6 +992,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       const int gtid = (dq & 3) * 32 + lane;
       const int t = gtid & 63, hf = gtid >> 6;
       const unsigned char* src = reinterpret_cast<const unsigned char*>(grp ? p.v : p.k);
+      const unsigned char* dsrc = reinterpret_cast<const unsigned char*>(grp ? p.dv : p.dk);
       // A failed wait does not leave the loop (no named barrier here, but
       // the stores must stay out of buffers an MMA may still read).
       bool ok = true;
@@ -993,9 +1001,11 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
         const int t0 = slo + i * kNT;
         const int tok = t0 + t;
         const bool live = ok && tok < shi;
-        const int blk = live ? p.block_table[(long long)s * p.max_blocks + tok / kPage] : 0;
+        const bool draft = scratch && tok >= ctx;  // from the tree scratch KV
+        const int blk = live && !draft ? p.block_table[(long long)s * p.max_blocks + tok / kPage] : 0;
         const unsigned char* row =
-            src + (((long long)blk * p.KVH + kvh) * kPage + tok % kPage) * C::RB;
+            draft ? dsrc + scratch_row(p, row0, kvh, tok - ctx) * C::RB
+                  : src + (((long long)blk * p.KVH + kvh) * kPage + tok % kPage) * C::RB;
         DqRaw<D> raw;
         dq_load<D>(raw, row, hf, live);
         // The group's first thread keeps its tensor kPrefetch tiles ahead in

@@ -109,6 +109,9 @@ class VerifyCase:
     page_size: int = 0
     capacity: int = 0
     block_table: Optional[np.ndarray] = None
+    # Optional tree scratch KV: [total_rows][KVH][row] storage rows.
+    draft_k: Optional[np.ndarray] = None
+    draft_v: Optional[np.ndarray] = None
     scale: float = 0.0
     num_splits: int = 1
     seed: int = 0
@@ -383,6 +386,92 @@ def mixed_prefill(num_splits: int = 8, seed: int = 1006, ctx=(8192, 16383, 20676
                      kv_dtype=Q8_0, q_dtype=BF16, ctx=list(ctx), rows=list(rows),
                      kinds=list(kinds), mode="mixed", paged=True, seed=seed,
                      num_splits=num_splits)
+
+
+def _cache_index(case: VerifyCase, s: int, kvh: int, t: int):
+    """Index tuple of token t of (s, kvh) in the case's cache array."""
+    if case.page_size == 0:
+        return (s, kvh, t)
+    return (int(case.block_table[s, t // PAGE]), kvh, t % PAGE)
+
+
+def with_tree_scratch(case: VerifyCase) -> VerifyCase:
+    """The same launch with the tree sequences' draft K/V moved into a tree
+    scratch KV [total_rows][KVH][row] (row r of the launch), their old cache
+    rows overwritten with NaN patterns, and the scratch rows of the other
+    sequences NaN too: a correct reader sees the same values as before and
+    never touches a NaN."""
+    relems = case.k.shape[-1]
+    poison = _poison_row(case.kv_dtype, relems)
+    k, v = case.k.copy(), case.v.copy()
+    dk = np.empty((case.total_rows, case.num_kv_heads, relems), dtype=case.k.dtype)
+    dv = np.empty_like(dk)
+    dk[:] = poison
+    dv[:] = poison
+    for s in range(case.num_seqs):
+        if case.seq_kind[s] != 1 and case.mode != "tree":
+            continue
+        lo, hi = int(case.cu_rows[s]), int(case.cu_rows[s + 1])
+        ctx = int(case.ctx_len[s])
+        for a in range(hi - lo):
+            for kvh in range(case.num_kv_heads):
+                idx = _cache_index(case, s, kvh, ctx + a)
+                dk[lo + a, kvh] = k[idx]
+                dv[lo + a, kvh] = v[idx]
+                k[idx] = poison
+                v[idx] = poison
+    return replace(case, k=k, v=v, draft_k=dk, draft_v=dv, name=case.name + "-scratch")
+
+
+def accepted_paths(case: VerifyCase, seed: int):
+    """Seeded accepted prefixes: for each tree sequence a root path ending
+    at a random node (or empty), none for chain sequences.  Returns int32
+    accepted_len [num_seqs] and accepted_nodes [total_rows] (root first,
+    -1 past each path)."""
+    rng = rng_for(seed)
+    acc_len = np.zeros(case.num_seqs, dtype=np.int32)
+    nodes = np.full(case.total_rows, -1, dtype=np.int32)
+    for s in range(case.num_seqs):
+        lo, hi = int(case.cu_rows[s]), int(case.cu_rows[s + 1])
+        tree = case.seq_kind[s] == 1 or case.mode == "tree"
+        if not tree or hi == lo:
+            continue
+        end = int(rng.integers(-1, hi - lo))  # -1: nothing accepted
+        path = []
+        while end >= 0:
+            path.append(end)
+            end = int(case.parent[lo + end])
+        path.reverse()
+        acc_len[s] = len(path)
+        nodes[lo:lo + len(path)] = path
+    return acc_len, nodes
+
+
+def accepted_as_chains(case: VerifyCase, k, v, acc_len, nodes) -> VerifyCase:
+    """A chain launch over a committed cache (k, v): one sequence per tree
+    sequence with an accepted path, its rows the path's query rows at
+    positions ctx .. ctx+m-1 (where the commit put their K/V)."""
+    seqs = [s for s in range(case.num_seqs) if acc_len[s] > 0]
+    qrows, ctx, rows = [], [], []
+    for s in seqs:
+        lo = int(case.cu_rows[s])
+        m = int(acc_len[s])
+        qrows += [lo + int(a) for a in nodes[lo:lo + m]]
+        ctx.append(int(case.ctx_len[s]))
+        rows.append(m)
+    cu = np.zeros(len(seqs) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(rows)
+    parent = np.concatenate([np.arange(-1, m - 1, dtype=np.int32) for m in rows])
+    if case.page_size:
+        bt = case.block_table[seqs]
+        kk, vv = k, v
+    else:
+        bt = None
+        kk, vv = k[seqs], v[seqs]
+    return replace(case, q=case.q[qrows], k=kk, v=vv, ctx_len=np.asarray(ctx, dtype=np.int32),
+                   cu_rows=cu, parent=parent, seq_kind=np.zeros(len(seqs), dtype=np.uint8),
+                   mode="chain", block_table=bt, draft_k=None, draft_v=None,
+                   name=case.name + "-accepted")
 
 
 def subset_sequences(case: VerifyCase, seqs) -> VerifyCase:

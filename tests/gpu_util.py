@@ -48,12 +48,13 @@ def q8_lse_bound(case):
         if hi == lo:
             continue
         ctx = int(case.ctx_len[s])
-        L = ctx + hi - lo
         kind = orc.seq_kind_of(s, case.seq_kind, case.mode)
+        draft = getattr(case, "draft_k", None) if kind == 1 else None
         for kvh in range(KVH):
-            K = orc.decode_rows(orc.kv_rows(case.k, s, kvh, L, page_size=case.page_size,
-                                            capacity=case.capacity, num_kv_heads=KVH,
-                                            block_table=case.block_table), case.kv_dtype)
+            K = orc.decode_rows(orc.span_rows(case.k, draft, s, kvh, ctx, hi - lo, lo,
+                                              page_size=case.page_size, capacity=case.capacity,
+                                              num_kv_heads=KVH, block_table=case.block_table),
+                                case.kv_dtype)
             for r in range(lo, hi):
                 pos = orc.visible_positions(ctx, hi - lo, kind, case.parent[lo:hi], r - lo)
                 for h in range(kvh * G, (kvh + 1) * G):

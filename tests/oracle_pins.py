@@ -266,13 +266,18 @@ def brute_force(case):
                 for t in range(L):
                     if not _bf_visible(t, ctx, j, kind, par):
                         continue
-                    if case.page_size:
-                        blk = int(case.block_table[s][t // 16])
-                        idx = (blk * KVH + kvh) * 16 + t % 16
+                    if getattr(case, "draft_k", None) is not None and kind == 1 and t >= ctx:
+                        # tree scratch KV: row lo + (t - ctx), this KV head
+                        kv = _bf_decode(case.kv_dtype, case.draft_k[lo + t - ctx][kvh])
+                        vv = _bf_decode(case.kv_dtype, case.draft_v[lo + t - ctx][kvh])
                     else:
-                        idx = (s * KVH + kvh) * case.capacity + t
-                    kv = _bf_decode(case.kv_dtype, kflat[idx])
-                    vv = _bf_decode(case.kv_dtype, vflat[idx])
+                        if case.page_size:
+                            blk = int(case.block_table[s][t // 16])
+                            idx = (blk * KVH + kvh) * 16 + t % 16
+                        else:
+                            idx = (s * KVH + kvh) * case.capacity + t
+                        kv = _bf_decode(case.kv_dtype, kflat[idx])
+                        vv = _bf_decode(case.kv_dtype, vflat[idx])
                     z = case.scale * sum(a * b for a, b in zip(qv, kv))
                     w = math.exp(z)
                     den += w
@@ -299,6 +304,11 @@ def brute_cases():
         sy.make_case("bf-f32-prefill-mixed", num_heads=2, num_kv_heads=1, head_dim=8,
                      kv_dtype=sy.F32, q_dtype=sy.F32, ctx=[3, 6], rows=[40, 5], kinds=[0, 1],
                      mode="mixed", seed=25),
+        # Tree drafts in a tree scratch KV (their cache rows NaN).
+        sy.with_tree_scratch(sy.make_case(
+            "bf-q8-mixed-paged-scratch", num_heads=4, num_kv_heads=2, head_dim=32,
+            kv_dtype=sy.Q8_0, q_dtype=sy.BF16, ctx=[17, 1, 0, 9], rows=[5, 1, 3, 6],
+            kinds=[1, 0, 1, 0], mode="mixed", paged=True, seed=26, extra_blocks=2)),
     ]
 
 
@@ -385,3 +395,72 @@ def check_direct_rows_independent_of_launch():
     d = sy.subset_sequences(c, [0, 1])
     Od, Ld = orc.verify_case(d)
     assert np.array_equal(O[:2], Od) and np.array_equal(LSE[:2], Ld)
+
+
+# ---------------------------------------------------------------------------
+# Tree commit of the KV (lucebox PR #686, "State and commit invariants").
+
+def _commit_args(ctx, parent, path, kind=1):
+    n = len(parent)
+    nodes = np.full(n, -1, dtype=np.int32)
+    nodes[:len(path)] = path
+    return dict(ctx_len=np.array([ctx]), cu_rows=np.array([0, n]),
+                parent=np.asarray(parent, dtype=np.int32), seq_kind=np.array([kind], np.uint8),
+                mode="mixed", accepted_len=np.array([len(path)], dtype=np.int32),
+                accepted_nodes=nodes)
+
+
+def check_tree_commit_golden():
+    g = load("tree_commit.json")
+    c = g["contiguous"]
+    scratch = np.asarray(c["scratch"], dtype=np.float32)[:, None, :]
+    for case in c["cases"]:
+        cap = case["capacity"]
+        cache = np.asarray(c["cache"][:cap], dtype=np.float32)[None, None]
+        k2, v2, bad = orc.promote(cache, cache, scratch, scratch, page_size=0, capacity=cap,
+                                  num_kv_heads=1, **_commit_args(c["ctx"], c["parent"],
+                                                                 case["path"]))
+        if "reason" in case:
+            assert bad == {case["reason"]}, (case["name"], bad)
+            assert np.array_equal(k2, cache) and np.array_equal(v2, cache), case["name"]
+        else:
+            assert not bad, (case["name"], bad)
+            assert np.array_equal(k2[0, 0], np.asarray(case["after"], np.float32)), case["name"]
+    pg = g["paged"]
+    pool = np.zeros((pg["num_blocks"], 1, 16, 2), dtype=np.float32)
+    scratch = np.asarray(pg["scratch"], dtype=np.float32)[:, None, :]
+    bt = np.asarray([pg["block_table"]], dtype=np.int32)
+    k2, _, bad = orc.promote(pool, pool, scratch, scratch, page_size=16, capacity=0,
+                             num_kv_heads=1, block_table=bt,
+                             **_commit_args(pg["ctx"], pg["parent"], pg["path"]))
+    assert not bad
+    want = np.zeros_like(pool)
+    for blk, slot, row in pg["written"]:
+        want[blk, 0, slot] = row
+    assert np.array_equal(k2, want)
+
+
+def check_commit_then_chain():
+    """Each accepted tree row (its drafts in the scratch KV) equals, exactly,
+    the same query as a chain row over the committed cache: the chain row
+    at position ctx + i sees the path's first i + 1 nodes, which are the
+    tree row's ancestors and itself, in the same order."""
+    base = sy.make_case("commit-chain", num_heads=4, num_kv_heads=2, head_dim=16,
+                        kv_dtype=sy.BF16, q_dtype=sy.BF16, ctx=[5, 12, 3], rows=[8, 1, 8],
+                        kinds=[1, 0, 1], mode="mixed", paged=True, seed=27)
+    c = sy.with_tree_scratch(base)
+    acc, nodes = sy.accepted_paths(c, 28)
+    O, L = orc.verify_case(c)
+    k2, v2, bad = orc.promote(c.k, c.v, c.draft_k, c.draft_v, ctx_len=c.ctx_len,
+                              cu_rows=c.cu_rows, parent=c.parent, seq_kind=c.seq_kind,
+                              mode=c.mode, accepted_len=acc, accepted_nodes=nodes,
+                              page_size=c.page_size, capacity=c.capacity,
+                              num_kv_heads=c.num_kv_heads, block_table=c.block_table)
+    assert not bad
+    ch = sy.accepted_as_chains(c, k2, v2, acc, nodes)
+    Oc, Lc = orc.verify_case(ch)
+    rows = [int(c.cu_rows[s]) + int(a) for s in range(c.num_seqs)
+            for a in nodes[int(c.cu_rows[s]):int(c.cu_rows[s]) + int(acc[s])]]
+    assert len(rows) == ch.total_rows > 0
+    assert np.array_equal(O[rows], Oc) and np.array_equal(L[rows], Lc)
+

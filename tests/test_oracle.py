@@ -10,7 +10,8 @@ import oracle_pins as P
     "check_split_rule_properties", "check_gather_golden", "check_paged_equals_contiguous",
     "check_golden_attention", "check_brute_force", "check_weights_sum_to_one",
     "check_closed_forms", "check_split_invariance", "check_chain_is_tree_with_chain_parents",
-    "check_direct_rows_independent_of_launch",
+    "check_direct_rows_independent_of_launch", "check_tree_commit_golden",
+    "check_commit_then_chain",
 ])
 def test_pin(name):
     getattr(P, name)()

@@ -13,6 +13,7 @@ ALL_PINS = [
     P.check_split_golden, P.check_gather_golden, P.check_paged_equals_contiguous,
     P.check_golden_attention, P.check_brute_force, P.check_closed_forms,
     P.check_split_invariance, P.check_chain_is_tree_with_chain_parents,
+    P.check_tree_commit_golden, P.check_commit_then_chain,
 ]
 
 
@@ -83,9 +84,42 @@ def _gather_slot_swapped(s, kvh, t, *, page_size, capacity, num_kv_heads, block_
     return (blk * num_kv_heads + kvh) * 16 + (15 - t % 16)
 
 
+def _promote_one_late(k, v, draft_k, draft_v, **kw):
+    kw["ctx_len"] = np.asarray(kw["ctx_len"]) + 1
+    return _orig["promote"](k, v, draft_k, draft_v, **kw)
+
+
+def _preflight_ignores_parents(**kw):
+    kw["parent"] = _fake_root_paths(kw["parent"], kw["accepted_nodes"], kw["cu_rows"],
+                                    kw["accepted_len"])
+    return _orig["promote_preflight"](**kw)
+
+
+def _fake_root_paths(parent, nodes, cu_rows, acc_len):
+    """A parent array under which every accepted path is a root path."""
+    par = np.array(parent, copy=True)
+    for s in range(len(cu_rows) - 1):
+        lo = int(cu_rows[s])
+        prev = -1
+        for i in range(int(acc_len[s])):
+            a = int(nodes[lo + i])
+            if 0 <= a < int(cu_rows[s + 1]) - lo:
+                par[lo + a] = prev
+            prev = a
+    return par
+
+
+def _span_rows_scratch_shifted(cache, draft, s, kvh, ctx, n, lo, **kw):
+    if draft is None:
+        return _orig["span_rows"](cache, None, s, kvh, ctx, n, lo, **kw)
+    shifted = np.roll(np.asarray(draft), -1, axis=0)
+    return _orig["span_rows"](cache, shifted, s, kvh, ctx, n, lo, **kw)
+
+
 _orig = {name: getattr(orc, name) for name in
          ["attend", "visible_positions", "ancestors", "kv_head_of", "dequant_q8_0",
-          "decode_fp16", "split_ranges", "merge", "gather_index"]}
+          "decode_fp16", "split_ranges", "merge", "gather_index", "promote",
+          "promote_preflight", "span_rows"]}
 
 MUTATIONS = {
     "scale dropped": ("attend", _attend_no_scale),
@@ -100,6 +134,9 @@ MUTATIONS = {
     "split chunk not page-rounded": ("split_ranges", _split_no_rounding),
     "merge without rescale": ("merge", _merge_no_rescale),
     "page slot reversed": ("gather_index", _gather_slot_swapped),
+    "commit lands one position late": ("promote", _promote_one_late),
+    "commit preflight ignores the tree": ("promote_preflight", _preflight_ignores_parents),
+    "scratch rows off by one": ("span_rows", _span_rows_scratch_shifted),
 }
 
 
