@@ -21,15 +21,18 @@ constexpr int kMergeThreads = 256;
 
 // One CTA per (row, head): D/4 column threads x (256 / (D/4)) slot groups.
 // Group g takes slots g, g + NG, ... in ascending order and issues every
-// load of its slots (m, l and a float4 of acc) before using any, so the
-// merge costs one round trip to the partials.  Each group keeps its own
+// load of its slots (m, l and a float4 of acc, up to BATCH at once) before
+// using any, so the merge costs one round trip to the partials up to
+// NG x BATCH slots (40 at D = 256: the 38 of a long-context call).  The
+// register cap keeps three CTAs on an SM, so a call's merge CTAs (384 at
+// 16 rows x 24 heads) run in one wave on 152 SMs.  Each group keeps its own
 // maximum M_g; the groups are then combined in ascending group order with
 // the overall maximum M:  l = sum_g 2^(M_g - M) l_g, acc likewise.
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
+__global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const Params p) {
   constexpr int TC = D / 4;
   constexpr int NG = kMergeThreads / TC;
-  constexpr int BATCH = 12;  // slots per group loaded together
+  constexpr int BATCH = 10;  // slots per group loaded together
   __shared__ float4 red[NG][TC];
   __shared__ float lred[NG], mred[NG];
   // Launched as a programmatic dependent of the partial kernel: wait here
