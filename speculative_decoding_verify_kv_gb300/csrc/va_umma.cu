@@ -477,6 +477,10 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     issue_q8(0, 1);
   };
   const bool early = Q8 && p.page_size == 0 && !err && ntiles > 0;
+  constexpr int kQRow = D * 2 + 16;
+  const int qslot = (min(kM, R - rb * kM) * kQRow <= 2 * C::TILE) ? 4 : 2;
+  unsigned char* const qstage = sm + qslot * C::TILE;
+  const int qfirst = qslot / 2;  // first tile whose buffers hold the staging
 
   if (tid == 0) {
     err_s = 0;
@@ -508,12 +512,13 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     fence_barrier_init();
     if (early) issue_first();
   }
-  // Q8: warps 2.. stage this CTA's Q rows in shared memory (tile buffers
-  // K1 onwards; rows padded to kQRow bytes so that the lanes of a warp read
-  // distinct bank groups) with every load in flight, overlapping the rest of
-  // the prologue; the softmax warps convert them into TMEM, and the
-  // producer loads tile 1 there only after Q is ready.
-  constexpr int kQRow = D * 2 + 16;
+  // Q8: warps 2.. stage this CTA's Q rows in shared memory (rows padded to
+  // kQRow bytes so that the lanes of a warp read distinct bank groups) with
+  // every load in flight, overlapping the rest of the prologue; the softmax
+  // warps convert them into TMEM.  The staging takes tile buffers K2 V2
+  // when the block's rows fit there (tile 1 then goes out as soon as tile 0
+  // has landed), else K1 onwards; tiles from qfirst on wait until Q is in
+  // TMEM.
   if (Q8 && warp >= 2) {
     constexpr int CPR = D / 8;  // 16-byte chunks per row
     constexpr int NTHR = C::THREADS - 64;
@@ -535,7 +540,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     for (int k = 0; k < ITER; ++k) {
       const int c = t + k * NTHR;
       if (c < total)
-        *reinterpret_cast<uint4*>(sm + 2 * C::TILE + (c / CPR) * kQRow + (c % CPR) * 16) = v[k];
+        *reinterpret_cast<uint4*>(qstage + (c / CPR) * kQRow + (c % CPR) * 16) = v[k];
     }
     named_barrier_sync(2, NTHR);
   }
@@ -608,10 +613,13 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
             prefetch_q8(i, 1);
           }
         }
-        // Buffers K1.. hold the Q staging until the softmax warps have put
-        // Q into TMEM.
-        if (ntiles > 1 && !mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs)) fail();
         for (int i = 1; i < ntiles && !*abort_p; ++i) {
+          // The buffers of tiles qfirst.. hold the Q staging until the
+          // softmax warps have put Q into TMEM.
+          if (i == qfirst && !mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs)) {
+            fail();
+            break;
+          }
           const int jb = i % C::NB16;
           const uint32_t par = ((i / C::NB16) & 1) ^ 1;
           bool ok = mbar_wait(bar(B_QEMPTY + jb), par, abort_p, kWaitNs);
@@ -785,7 +793,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       // Q8: from the shared staging copy (rows padded so the lanes of a warp
       // hit distinct bank groups); bf16: straight from global memory.
       const uint4* qsrc =
-          Q8 ? reinterpret_cast<const uint4*>(sm + 2 * C::TILE + r * kQRow + half * D)
+          Q8 ? reinterpret_cast<const uint4*>(qstage + r * kQRow + half * D)
              : reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(p.q) +
                                               ((long long)grow * p.H + h) * D + half * (D / 2));
       float qscale = 1.f;
@@ -985,8 +993,8 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       // their tensor's tiles at their own pace (warp 18 is idle, 13 issues
       // the P.V MMAs).  Per tile: load the raw half-row from global memory, wait
       // until the tile buffer is free (the MMA that read its previous tile
-      // has completed; tiles 1 and 2 also wait for Q to have left the
-      // staging area), convert, store, release.
+      // has completed; tiles from qfirst on also wait for Q to have left
+      // the staging area), convert, store, release.
       const int dq = dq_slot(warp);
       const int grp = dq >> 2;  // 0 = K, 1 = V
       const int gtid = (dq & 3) * 32 + lane;
@@ -1017,7 +1025,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
         if (ok && !__all_sync(0xffffffffu,
                               mbar_wait(bar(B_QEMPTY + 3 * grp + jb), ((i / C::NB16) & 1) ^ 1,
                                         abort_p, kWaitNs) &&
-                                  (i == 0 || mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs)))) {
+                                  (i < qfirst || mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs)))) {
           ok = false;
           if (lane == 0) fail();
         }
