@@ -63,11 +63,12 @@ def _problem(**kw):
 
 def _kv(**kw):
     d = dict(dtype=va.Q8_0, num_kv_heads=4, head_dim=256, k=FAKE, v=FAKE, page_size=0,
-             capacity=32784, block_table=None, max_blocks_per_seq=0, num_blocks=0)
+             capacity=32784, block_table=None, max_blocks_per_seq=0, num_blocks=0,
+             draft_k=None, draft_v=None)
     d.update(kw)
     return va.VaKV(d["dtype"], d["num_kv_heads"], d["head_dim"], d["k"], d["v"],
                    d["page_size"], d["capacity"], d["block_table"], d["max_blocks_per_seq"],
-                   d["num_blocks"])
+                   d["num_blocks"], d["draft_k"], d["draft_v"])
 
 
 def validate(p, kv, mode=va.MODE_CHAIN, ws=1 << 40):
@@ -153,3 +154,24 @@ def test_plan_does_not_depend_on_other_sequences():
 
     assert info(num_seqs=2, total_rows=2, max_rows_per_seq=1) == \
         info(num_seqs=8, total_rows=50, max_rows_per_seq=8)
+
+
+def test_promote_host_checks():
+    """verify_attn_promote rejects missing arguments before any device
+    access: the tree scratch KV, accepted_len and the status word are
+    required, and the usual problem checks apply."""
+    P = ctypes.c_void_p
+    fn = va.lib.verify_attn_promote
+
+    def call(p, kv, acc=FAKE, nodes=FAKE, status=FAKE):
+        return fn(ctypes.byref(p), ctypes.byref(kv), va.MODE_MIXED, P(acc), P(nodes), P(status),
+                  None)
+
+    scratch = dict(draft_k=FAKE, draft_v=FAKE)
+    assert call(_problem(), _kv()) == 1                                   # no scratch KV
+    assert call(_problem(), _kv(**scratch), acc=None) == 1               # no accepted_len
+    assert call(_problem(), _kv(**scratch), status=None) == 1            # no status word
+    assert call(_problem(), _kv(**scratch), nodes=None) == 1             # rows but no nodes
+    assert call(_problem(num_heads=25), _kv(**scratch)) == 2             # problem checks
+    assert call(_problem(), _kv(draft_k=FAKE, draft_v=None)) == 1        # half a scratch KV
+    assert call(_problem(), _kv(draft_k=FAKE + 8, draft_v=FAKE)) == 3    # unaligned scratch
