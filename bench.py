@@ -502,6 +502,7 @@ def run_ours(args):
         for name, make in [("dflash-bf16 ctx4096 S8", lambda: sy.dflash_bf16(ctx=4096, num_splits=8)),
                            ("dflash-bf16 ctx8192 S8", lambda: sy.dflash_bf16(ctx=8192, num_splits=8)),
                            ("paged-d128 bf16 4x~29K S8", lambda: sy.paged_d128()),
+                           ("paged-d128 Q8 4x~29K S8", lambda: sy.paged_d128(kv_dtype=sy.Q8_0)),
                            ("mixed tree+direct Q8 paged S8", lambda: sy.mixed_tree_direct()),
                            ("mixed prefill-256+direct+tree Q8 paged S8", lambda: sy.mixed_prefill())]:
             c3 = make()

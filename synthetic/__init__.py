@@ -348,14 +348,16 @@ def long_q8(ctx: int = 32768, num_splits: int = 8, seed: int = 1003) -> VerifyCa
                      num_splits=num_splits)
 
 
-def paged_d128(num_splits: int = 8, seed: int = 1004, ctx=None) -> VerifyCase:
+def paged_d128(num_splits: int = 8, seed: int = 1004, ctx=None,
+               kv_dtype: str = BF16) -> VerifyCase:
     """4 sequences, ctx ~ U{28000..30000}, H32/KV8/D128, 16 chain rows each,
-    bf16 N(0,1), 16-token pages under a shuffled block table."""
+    bf16 N(0,1) (or Q8_0 with kv_dtype), 16-token pages under a shuffled
+    block table."""
     if ctx is None:
         r = rng_for(seed + 7)
         ctx = [int(c) for c in r.integers(28000, 30001, size=4)]
-    return make_case("paged-d128-bf16", num_heads=32, num_kv_heads=8, head_dim=128,
-                     kv_dtype=BF16, q_dtype=BF16, ctx=list(ctx), rows=[16] * len(ctx),
+    return make_case("paged-d128-" + kv_dtype, num_heads=32, num_kv_heads=8, head_dim=128,
+                     kv_dtype=kv_dtype, q_dtype=BF16, ctx=list(ctx), rows=[16] * len(ctx),
                      paged=True, seed=seed, num_splits=num_splits)
 
 

@@ -292,6 +292,15 @@ def test_workload_paged_d128():
     sampled(sy.paged_d128(), 8)
 
 
+def test_workload_paged_d128_q8():
+    """The batched D=128 shape over a paged Q8_0 cache (the Q8 D=128 path)."""
+    c = sy.paged_d128(kv_dtype=sy.Q8_0)
+    rows, heads = sample_rows_heads(c)
+    o, lse = run_gpu(c, num_splits=8)
+    O, L = oracle.verify_case(c, rows=rows, heads=heads)
+    compare(o, lse, O, L, f"{c.name} S=8 (sampled)", lse_tol=q8_lse_bound(c))
+
+
 def test_workload_mixed_tree_direct():
     c = sy.mixed_tree_direct()
     sampled(c, 8)
