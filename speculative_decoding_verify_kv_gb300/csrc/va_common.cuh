@@ -15,7 +15,6 @@ constexpr int kPage = 16;
 constexpr int kChunkAlign = 64;  // KV chunks are whole 64-token tiles
 constexpr int kQ8Block = 32;
 constexpr int kQ8BlockBytes = 34;
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Everything a partial / merge / debug kernel needs, passed by value.

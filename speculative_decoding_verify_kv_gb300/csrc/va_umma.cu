@@ -58,7 +58,6 @@ struct UCfg {
   static constexpr int NB = D / 32;                      // Q8 blocks per row
   static constexpr int DBLK = D / 64;                    // 64-element column blocks
   static constexpr int TILE = kNT * D * 2;               // one 16-bit tile in smem
-  static constexpr int RAW_HALF = kNT * RB;              // raw K (or V) bytes of a tile
   static constexpr int NB16 = 3;                         // Q8 tile buffers per tensor
   static constexpr int NST = (D == 256) ? 3 : (D == 128 ? 6 : 8);  // bf16 K+V stages
   static constexpr int COL_O = 0;
