@@ -24,6 +24,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import subprocess
 import sys
 import tempfile
@@ -68,21 +69,30 @@ def parse():
 
 # DRAM bytes (read + write) of one tensor-core partial launch on the
 # ctx-32768 workload, from the full ncu capture summarised under profiles/.
-# Reported only while the kernel sources are the ones it was taken on.
+# Reported only while the kernel sources (comments and white space aside)
+# are the ones it was taken on.
 PROFILED_TRAFFIC = {
     "bytes": 73_513_984,
-    "sources": {"va_umma.cu": "22a9678911daa4a7", "va_common.cuh": "046b7cc8ab917bd6",
-                "va_sm100.cuh": "6a151d6653b31471"},
+    "sources": {"va_umma.cu": "03910589e6bcca2d", "va_common.cuh": "69f96982534defe0",
+                "va_sm100.cuh": "5d2883a00bf72a31"},
 }
 
 
-def profiled_traffic():
+def _code_hash(text: str) -> str:
+    """Hash of a C++/CUDA source with comments and white space removed."""
     import hashlib
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    text = re.sub(r"\s+", "", text)
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
+
+
+def profiled_traffic():
     csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)),
                         "speculative_decoding_verify_kv_gb300", "csrc")
     for name, want in PROFILED_TRAFFIC["sources"].items():
-        with open(os.path.join(csrc, name), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest()[:16] != want:
+        with open(os.path.join(csrc, name)) as f:
+            if _code_hash(f.read()) != want:
                 return None
     return PROFILED_TRAFFIC["bytes"]
 

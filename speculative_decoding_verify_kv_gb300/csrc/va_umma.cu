@@ -9,7 +9,8 @@
 //
 //   S = Q K^T      tcgen05.mma, A = Q (TMEM), B = K tile (smem, K-major)
 //   softmax        8 warps, one TMEM lane (= query row) per thread and one
-//                  half of the tile's columns per warp; masks; online
+//                  half of the tile's columns per warp; masks (chain rows
+//                  causal by index, tree rows by ancestor mask); online
 //                  (m, l) in log2 units; P written back over S
 //   O += P V       tcgen05.mma, A = P (TMEM), B = V tile (smem, MN-major)
 //
@@ -24,7 +25,8 @@
 //     them in place to fp16 (one rounding of d*q) in the 128-byte-swizzled
 //     MMA layout, zero-filling tokens past the range.  Paged (a separate
 //     instantiation): the same warps load the raw rows themselves through
-//     the block table.  Q is converted to fp16 after a per-row power-of-two
+//     the block table (a tree sequence's drafts from the tree scratch KV
+//     when one is given).  Q is converted to fp16 after a per-row power-of-two
 //     rescale (exact), and the scale folds into the score multiplier.  P
 //     is fp16.
 //   bf16: tiled TMA loads place K/V tiles directly in the MMA layout; one
