@@ -79,3 +79,22 @@ def test_workload_mixed_prefill():
     o, lse = run_gpu(c, num_splits=8)
     O, L = oracle.verify_case(c, rows=rows, heads=heads)
     compare(o, lse, O, L, f"{c.name} S=8 (sampled)")
+
+
+@pytest.mark.parametrize("flags", KERNELS)
+def test_prefill_at_the_row_limit(flags):
+    """A chain of VA_MAX_ROWS_PER_SEQ (1,024) rows: 32 row blocks of 128
+    MMA rows at G = 4, ragged context."""
+    assert va.MAX_ROWS_PER_SEQ == 1024
+    c = sy.make_case("prefill-1024", num_heads=4, num_kv_heads=1, head_dim=64,
+                     kv_dtype=sy.BF16, q_dtype=sy.BF16, ctx=[77], rows=[1024], seed=305)
+    _full(c, 2, flags)
+
+
+def test_prefill_chain_q8_contiguous_g8():
+    """A 100-row chain at G = 8 (7 row blocks) over a contiguous Q8_0 cache
+    with a multi-tile context, beside a direct row."""
+    c = sy.make_case("prefill-q8-g8", num_heads=16, num_kv_heads=2, head_dim=128,
+                     kv_dtype=sy.Q8_0, q_dtype=sy.BF16, ctx=[700, 300], rows=[100, 1],
+                     seed=306)
+    _full(c, 3, 0)
