@@ -233,7 +233,8 @@ va_status verify_attn_mixed(const va_problem *p, const va_kv *kv, void *ws, size
  * Debug export of the row map and masks the kernels use: row_seq[r] is the
  * sequence of global row r; anc_mask[r] has bit a set iff draft position a
  * of that sequence is visible to row r (itself or an ancestor).  Device
- * outputs of total_rows entries each.  (lucebox PR #686 "Correctness failure
+ * outputs of total_rows entries each.  The mask has 32 bits: a chain row
+ * j >= 31 gets every bit (the kernels decide chain visibility from j).  (lucebox PR #686 "Correctness failure
  * found during qualification": the compact row map and W8 topology checks.)
  */
 va_status va_debug_row_map(const va_problem *p, int32_t mode, int32_t *row_seq,
