@@ -119,10 +119,10 @@ static Plan make_plan(const va_problem* p, const va_kv* kv) {
   pl.rows_per_block = tensor ? kUmmaRowsPerBlock : kSimtRowsPerBlock;
   pl.threads = tensor ? umma_threads(kv->head_dim, kv->dtype) : kSimtThreadsPerBlock;
   pl.smem = tensor ? umma_smem_bytes(kv->head_dim, kv->dtype) : simt_smem_bytes(kv->head_dim);
-  // Each sequence's KV span is cut into `slots` equal 16-token-aligned
-  // chunks (fewer when the span is short), the count fixed by S, the KV
-  // head count and the SM count only: never by the other sequences of the
-  // launch.  One sequence's chunks of one KV head fill one wave of CTAs
+  // Each sequence's KV span is cut into at most `slots` chunks of whole
+  // 64-token tiles, at least 128 tokens each (fewer when the span is
+  // short), the count fixed by S, the KV head count and the SM count only:
+  // never by the other sequences of the launch.  One sequence's chunks of one KV head fill one wave of CTAs
   // (the tensor-core kernel holds one CTA per SM, the CUDA-core kernel
   // about two); the count is at least S and at most S * kMaxSubSplits.
   const int target = (tensor ? 1 : 2) * sm_count();
