@@ -46,6 +46,8 @@ UNIT = "GB/s"
 HEADLINE_CTX = 32768
 OTHER_CTX = [8192, 20676]
 SPLITS = 8
+KERNEL_NAMES = {0: "CUDA-core partial", 1: "tensor-core partial (rows on M)",
+                2: "tensor-core Q8 partial (tokens on M)"}
 
 
 def parse():
@@ -527,7 +529,7 @@ def run_ours(args):
             workloads[name] = {"us_per_call": us, "kv_bytes_per_call": c3.kv_bytes,
                                "kv_gbs": c3.kv_bytes / (us * 1e-6) / 1e9,
                                "hbm_frac": c3.kv_bytes / (us * 1e-6) / 1e9 / peak,
-                               "kernel": "tensor-core" if b3.plan["kernel"] == 1 else "CUDA-core",
+                               "kernel": KERNEL_NAMES[b3.plan["kernel"]],
                                "slots": b3.plan["slots"]}
             del b3
 
@@ -538,12 +540,12 @@ def run_ours(args):
 
     if rank != 0:
         return
-    kernel_name = "tensor-core partial" if b.plan["kernel"] == 1 else "CUDA-core partial"
+    kernel_name = KERNEL_NAMES[b.plan["kernel"]]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": per_call_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16" if b.plan["kernel"] == 1 else "f32",
+        "dtype": "f16" if b.plan["kernel"] != 0 else "f32",
         "data": "synthetic",
         "config": {"workload": f"long-context Q8 verify: 1 seq, B=16 chain, H24/KV4/D256, Q8_0 "
                                f"KV (bf16 Q), ctx {HEADLINE_CTX}, split-KV S={SPLITS}",
@@ -565,7 +567,7 @@ def run_ours(args):
         "workloads": workloads,
         "roofline": {"kernel": kernel_name, "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak if achieved else None,
-                     "traffic": profiled_traffic() if b.plan["kernel"] == 1 else None,
+                     "traffic": profiled_traffic() if b.plan["kernel"] == 2 else None,
                      "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one "
                                        "capture of this kernel (null once it has changed)",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",

@@ -252,8 +252,13 @@ va_status va_debug_gather_index(const va_problem *p, const va_kv *kv, int32_t kv
                                 void *stream);
 
 /* Plan details for a problem (which kernel runs, splits and sub-splits). */
+/* Partial kernels (va_plan_info.kernel). */
+#define VA_KERNEL_CUDA_CORES 0 /* fp32 FMA, one thread block per 16 query rows */
+#define VA_KERNEL_TENSOR 1     /* tcgen05, query rows on the MMA's M axis (bf16 caches) */
+#define VA_KERNEL_TENSOR_Q8 2  /* tcgen05, tokens on M and query rows on N (Q8_0 caches) */
+
 typedef struct va_plan_info {
-  int32_t kernel;          /* 0 = CUDA-core partial, 1 = tensor-core partial */
+  int32_t kernel;          /* VA_KERNEL_* */
   int32_t sub_splits;      /* T: KV chunks per sequence (equal to slots) */
   int32_t slots;           /* T partial slots per (row, head) */
   int32_t grid_x, grid_y, grid_z;

@@ -19,6 +19,8 @@ from . import _build
 F32, BF16, Q8_0 = 0, 1, 2
 MODE_CHAIN, MODE_TREE, MODE_MIXED = 0, 1, 2
 FLAG_CUDA_CORES = 0x1
+# Partial kernels (va_plan_info.kernel).
+KERNEL_CUDA_CORES, KERNEL_TENSOR, KERNEL_TENSOR_Q8 = 0, 1, 2
 
 DEV_BAD_PARENT = 0x1
 DEV_BAD_BLOCK = 0x2

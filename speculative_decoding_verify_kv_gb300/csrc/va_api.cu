@@ -21,6 +21,10 @@ int simt_smem_bytes(int D);
 cudaError_t launch_umma_partial(const Params& p, dim3 grid, cudaStream_t st);
 int umma_smem_bytes(int D, int kv_dtype);
 int umma_threads(int D, int kv_dtype);
+cudaError_t launch_tq8_partial(const Params& p, dim3 grid, cudaStream_t st);
+int tq8_rows_per_block();
+int tq8_threads();
+int tq8_smem_bytes(int D);
 
 static thread_local cudaError_t g_last_cuda = cudaSuccess;
 static va_status note_cuda(cudaError_t e) {
@@ -102,7 +106,7 @@ static va_status check(const va_problem* p, const va_kv* kv, int mode) {
 }
 
 struct Plan {
-  int kernel;  // 0 simt, 1 tensor-core
+  int kernel;  // VA_KERNEL_*
   int P, slots, rows_per_block, row_blocks, threads, smem;
   dim3 grid;
 };
@@ -110,15 +114,29 @@ struct Plan {
 static Plan make_plan(const va_problem* p, const va_kv* kv) {
   Plan pl;
   const int G = p->num_heads / kv->num_kv_heads;
-  // Kernel choice from the cache dtype and the caller's flag only.
-  // With a tree scratch KV the tensor-core kernel serves Q8_0 paged caches
-  // (its dequantising warps load each row through its own address).
-  const bool scratch_ok = !kv->draft_k || (kv->dtype == VA_Q8_0 && kv->page_size == kPage);
-  const bool tensor = kv->dtype != VA_F32 && !(p->flags & VA_FLAG_CUDA_CORES) && scratch_ok;
-  pl.kernel = tensor ? 1 : 0;
-  pl.rows_per_block = tensor ? kUmmaRowsPerBlock : kSimtRowsPerBlock;
-  pl.threads = tensor ? umma_threads(kv->head_dim, kv->dtype) : kSimtThreadsPerBlock;
-  pl.smem = tensor ? umma_smem_bytes(kv->head_dim, kv->dtype) : simt_smem_bytes(kv->head_dim);
+  // Kernel choice from the cache dtype, the caller's flag and whether a
+  // tree scratch KV is given, never from the problem's sizes: Q8_0 caches
+  // run on the transposed tensor-core kernel (any layout, with or without
+  // a scratch KV), bf16 caches on the row-major tensor-core kernel (no
+  // scratch KV), everything else on the CUDA-core kernel.
+  const bool tensor_ok = kv->dtype != VA_F32 && !(p->flags & VA_FLAG_CUDA_CORES);
+  if (tensor_ok && kv->dtype == VA_Q8_0) {
+    pl.kernel = VA_KERNEL_TENSOR_Q8;
+    pl.rows_per_block = tq8_rows_per_block();
+    pl.threads = tq8_threads();
+    pl.smem = tq8_smem_bytes(kv->head_dim);
+  } else if (tensor_ok && !kv->draft_k) {
+    pl.kernel = VA_KERNEL_TENSOR;
+    pl.rows_per_block = kUmmaRowsPerBlock;
+    pl.threads = umma_threads(kv->head_dim, kv->dtype);
+    pl.smem = umma_smem_bytes(kv->head_dim, kv->dtype);
+  } else {
+    pl.kernel = VA_KERNEL_CUDA_CORES;
+    pl.rows_per_block = kSimtRowsPerBlock;
+    pl.threads = kSimtThreadsPerBlock;
+    pl.smem = simt_smem_bytes(kv->head_dim);
+  }
+  const bool tensor = pl.kernel != VA_KERNEL_CUDA_CORES;
   // Each sequence's KV span is cut into at most `slots` chunks of whole
   // 64-token tiles, at least 128 tokens each (fewer when the span is
   // short), the count fixed by S, the KV head count and the SM count only:
@@ -232,6 +250,14 @@ static TimingSlot* timing_slot() {
   return &g_timing_slots[g_timing_next++];
 }
 
+static cudaError_t launch_partial(const Plan& pl, const Params& q, cudaStream_t cs) {
+  switch (pl.kernel) {
+    case VA_KERNEL_TENSOR_Q8: return launch_tq8_partial(q, pl.grid, cs);
+    case VA_KERNEL_TENSOR: return launch_umma_partial(q, pl.grid, cs);
+    default: return launch_simt_partial(q, pl.grid, cs);
+  }
+}
+
 static va_status run(const va_problem* p, const va_kv* kv, int mode, void* ws, size_t ws_bytes,
                      float* o, float* lse, uint32_t* status, void* stream) {
   va_status st = check(p, kv, mode);
@@ -249,8 +275,7 @@ static va_status run(const va_problem* p, const va_kv* kv, int mode, void* ws, s
   // External records so that, under stream capture, they become event
   // nodes of the graph (plain records only order work inside a capture).
   if (ts) timing_record(ts->e[0], cs);
-  cudaError_t e = pl.kernel == 1 ? launch_umma_partial(q, pl.grid, cs)
-                                 : launch_simt_partial(q, pl.grid, cs);
+  cudaError_t e = launch_partial(pl, q, cs);
   if (e != cudaSuccess) return note_cuda(e);
   if (ts) timing_record(ts->e[1], cs);
   e = launch_merge(q, cs);
@@ -463,7 +488,7 @@ va_status verify_attn_noalloc(const va_problem* p, const va_kv* kv, int32_t mode
   if (e != cudaSuccess) return note_cuda(e);
   Params q = make_params(p, kv, mode, pl, ws, o, lse, status);
   cudaStream_t cs = (cudaStream_t)stream;
-  e = pl.kernel == 1 ? launch_umma_partial(q, pl.grid, cs) : launch_simt_partial(q, pl.grid, cs);
+  e = launch_partial(pl, q, cs);
   if (e != cudaSuccess) return note_cuda(e);
   e = launch_merge(q, cs);
   if (e != cudaSuccess) return note_cuda(e);

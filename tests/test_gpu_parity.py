@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import synthetic as sy
-from gpu_util import compare, q8_lse_bound, run_gpu, sample_rows_heads
+from gpu_util import compare, run_gpu, sample_rows_heads
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -20,16 +20,12 @@ import speculative_decoding_verify_kv_gb300 as va  # noqa: E402
 KERNELS = [0, va.FLAG_CUDA_CORES]
 
 
-def full(case, flags=0, num_splits=None, what="", strict_lse=False):
-    """Every output against the oracle.  On the Q8 tensor-core path the LSE
-    bar is max(1e-4, the fp16-K rounding bound) unless ``strict_lse``."""
+def full(case, flags=0, num_splits=None, what=""):
+    """Every output against the oracle."""
     S = num_splits or case.num_splits
     o, lse = run_gpu(case, num_splits=S, flags=flags)
     O, L = oracle.verify_case(case)
-    tol = None
-    if case.kv_dtype == sy.Q8_0 and not (flags & va.FLAG_CUDA_CORES) and not strict_lse:
-        tol = q8_lse_bound(case)
-    return compare(o, lse, O, L, what or f"{case.name} S={S} flags={flags}", lse_tol=tol)
+    return compare(o, lse, O, L, what or f"{case.name} S={S} flags={flags}")
 
 
 # --------------------------------------------------------------------------
@@ -298,7 +294,7 @@ def test_workload_paged_d128_q8():
     rows, heads = sample_rows_heads(c)
     o, lse = run_gpu(c, num_splits=8)
     O, L = oracle.verify_case(c, rows=rows, heads=heads)
-    compare(o, lse, O, L, f"{c.name} S=8 (sampled)", lse_tol=q8_lse_bound(c))
+    compare(o, lse, O, L, f"{c.name} S=8 (sampled)")
 
 
 def test_workload_mixed_tree_direct():

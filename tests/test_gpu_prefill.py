@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 import synthetic as sy
-from gpu_util import compare, q8_lse_bound, run_gpu, sample_rows_heads
+from gpu_util import compare, run_gpu, sample_rows_heads
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -21,10 +21,7 @@ KERNELS = [0, va.FLAG_CUDA_CORES]
 def _full(case, S, flags):
     o, lse = run_gpu(case, num_splits=S, flags=flags)
     O, L = oracle.verify_case(case)
-    tol = None
-    if case.kv_dtype == sy.Q8_0 and not (flags & va.FLAG_CUDA_CORES):
-        tol = q8_lse_bound(case)
-    return compare(o, lse, O, L, f"{case.name} S={S} flags={flags}", lse_tol=tol)
+    return compare(o, lse, O, L, f"{case.name} S={S} flags={flags}")
 
 
 @pytest.mark.parametrize("flags", KERNELS)
