@@ -36,8 +36,9 @@
 // rounding) and P is fp16, as the P.V product's precision allows.
 //
 // Warp roles (16 warps, four warpgroups with their own register budgets):
-//   0 copy producer (raw Q8 rows into shared memory by 1-D bulk copies,
-//     L2 prefetch ahead), 1 TMEM owner + S^T issuer, 2 P.V issuer, 3 idle;
+//   0 and 3 copy producers of K and V (raw Q8 rows into shared memory by
+//     1-D bulk copies, L2 prefetch ahead), 1 TMEM owner + S^T issuer, 2 P.V
+//     issuer;
 //   4..7 softmax (warp & 3 = TMEM lane quadrant = 32 tokens, every row),
 //     also the O^T rescale and the epilogue;
 //   8..11 K dequantisation (one token row per thread, into TMEM);
@@ -62,6 +63,10 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kLaunchRegs = 128;  // 65536 registers / 512 threads
 constexpr int kPrefetch = 4;     // L2 prefetch distance in tiles
 constexpr uint64_t kWaitNs = 2000000000ull;
+// A row's running maximum m (log2 units) moves only when one of its scores
+// passes m + kSlack: P = 2^(s c - m) stays below 2^kSlack, well inside
+// fp16 (P^T) and fp32 (row sums, O^T).
+constexpr float kSlack = 14.f;
 
 // TMEM columns (512 allocated): O^T half h (d in [128h, 128h + 128)) at
 // COL_O + h*kNR; S^T buffer b at COL_S + b*kNR; K slot k at COL_K + 64k
@@ -73,7 +78,7 @@ constexpr int TMEM_COLS = 512;
 static_assert(COL_K + 128 <= TMEM_COLS, "TMEM map");
 
 // Warp roles.
-constexpr int W_PROD = 0, W_SMMA = 1, W_PV = 2;
+constexpr int W_PROD = 0, W_SMMA = 1, W_PV = 2, W_PRODV = 3;
 constexpr int W_SM0 = 4;    // softmax warps 4..7
 constexpr int W_KDQ0 = 8;   // K dequantisation warps 8..11
 constexpr int W_VDQ0 = 12;  // V dequantisation warps 12..15
@@ -82,7 +87,7 @@ constexpr int kRoleWarps = 4;  // warps per softmax / dequantisation role (one p
 // the registers the block is launched with (4 x kLaunchRegs), so the
 // softmax warpgroup's setmaxnreg.inc is covered by the other warpgroups'
 // decrements.
-constexpr int REG_CTRL = 80, REG_SM = 256, REG_KDQ = 96, REG_VDQ = 72;
+constexpr int REG_CTRL = 72, REG_SM = 256, REG_KDQ = 120, REG_VDQ = 56;
 static_assert(REG_CTRL + REG_SM + REG_KDQ + REG_VDQ <= 4 * kLaunchRegs, "register split");
 
 template <int D>
@@ -93,39 +98,37 @@ struct Cfg {
   static constexpr int DV = D < 128 ? 128 : D;      // V / O^T extent along d
   static constexpr int DH = DV / 128;               // O^T halves
   static constexpr int NFILL = D / 64;              // K slot fills (64 d each) per tile
-  static constexpr int NRAW = D == 256 ? 1 : 2;     // raw-row buffers per tensor
+  static constexpr int NRAW = D == 256 ? 1 : 2;     // raw V row buffers
   static constexpr int NVB = D == 256 ? 1 : 2;      // fp16 V tile buffers
   static constexpr int QT_BLK = kNR * 128;          // one 64-d column block of Q^T
   static constexpr int QT_BYTES = (D / 64) * QT_BLK;
   static constexpr int PT_BLK = kTT * 128;          // one 64-row block of P^T
-  static constexpr int PT_BYTES = 2 * PT_BLK;
+  static constexpr int PT_BYTES = 2 * PT_BLK;       // one P^T buffer (rows 0..127)
+  static constexpr int NPB = 2;                     // P^T buffers
   static constexpr int VT_BLK = kTT * 128;          // one 64-d column block of a V tile
   static constexpr int VT_BYTES = (DV / 64) * VT_BLK;
   static constexpr int RAW_BYTES = (kTT * RB + 127) / 128 * 128;
   static constexpr int OFF_QT = 0;
   static constexpr int OFF_PT = OFF_QT + QT_BYTES;
-  static constexpr int OFF_VT = OFF_PT + PT_BYTES;
-  static constexpr int OFF_RK = OFF_VT + NVB * VT_BYTES;
-  static constexpr int OFF_RV = OFF_RK + NRAW * RAW_BYTES;
+  static constexpr int OFF_VT = OFF_PT + NPB * PT_BYTES;
+  static constexpr int OFF_RV = OFF_VT + NVB * VT_BYTES;
   static constexpr int SMEM = OFF_RV + NRAW * RAW_BYTES + 1024;
 };
 
 enum {
-  B_RKF = 0,    // [2] raw K rows of the buffer's tile landed
-  B_RKE = 2,    // [2] raw K buffer read by the K dequantisation warps
-  B_RVF = 4,    // [2] raw V rows landed
-  B_RVE = 6,    // [2] raw V buffer read
-  B_KSF = 8,    // [2] K slot written (TMEM)
-  B_KSE = 10,   // [2] the S^T MMAs reading a K slot completed
-  B_STF = 12,   // [2] S^T of the buffer's tile complete
-  B_STE = 14,   // [2] S^T buffer read by the softmax
-  B_PF = 16,    // P^T written
-  B_PE = 17,    // the P.V MMAs of the last tile completed
-  B_VF = 18,    // [2] fp16 V tile written
-  B_VE = 20,    // [2] V tile free again
-  B_OF = 22,    // the last P.V completed
-  B_DRAIN = 23, // [2] S^T issuer, P.V issuer
-  B_COUNT = 25
+  B_RVF = 0,    // [2] raw V rows of the buffer's tile landed
+  B_RVE = 2,    // [2] raw V buffer read by the V dequantisation warps
+  B_KSF = 4,    // [2] K slot written (TMEM)
+  B_KSE = 6,    // [2] the S^T MMAs reading a K slot completed
+  B_STF = 8,    // [2] S^T of the buffer's tile complete
+  B_STE = 10,   // [2] S^T buffer read by the softmax
+  B_PF = 12,    // [2] P^T buffer written
+  B_PE = 14,    // [2] the P.V MMAs reading a P^T buffer completed
+  B_VF = 16,    // [2] fp16 V tile written
+  B_VE = 18,    // [2] V tile free again
+  B_OF = 20,    // the last P.V completed
+  B_DRAIN = 21, // [2] S^T issuer, P.V issuer
+  B_COUNT = 23
 };
 
 // Byte offset of 16-byte chunk `chunk` (< 8) of row `row` inside a
@@ -228,6 +231,7 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
   __shared__ __align__(16) float2 cm_s[kNR];
   __shared__ __align__(16) float m_s[kNR];
   __shared__ __align__(16) float thr_s[kNR];
+  __shared__ float rc_s[kNR];            // 1 / c (0 for padded rows)
   __shared__ __align__(16) float f_s[kNR];
   __shared__ long long slot_s[kNR];      // partial slot index of each row
   __shared__ int jr_s[kNR];              // local row index (in the sequence) of each row
@@ -272,9 +276,8 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   unsigned char* const qt = sm + C::OFF_QT;
-  unsigned char* const pt = sm + C::OFF_PT;
+  auto ptb = [&](int b) { return sm + C::OFF_PT + b * C::PT_BYTES; };
   auto vt = [&](int b) { return sm + C::OFF_VT + b * C::VT_BYTES; };
-  auto rawk = [&](int b) { return sm + C::OFF_RK + b * C::RAW_BYTES; };
   auto rawv = [&](int b) { return sm + C::OFF_RV + b * C::RAW_BYTES; };
 
   // Raw-row copies of tile i of tensor kv (0 = K, 1 = V): the cache tokens
@@ -311,13 +314,13 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
                            kPage * C::RB);
     }
   };
-  auto issue = [&](int i, int kv, uint64_t pol) {
+  auto issue_v = [&](int i, uint64_t pol) {
     int t0, nload;
     tile_span(i, &t0, &nload);
     const int b = i % C::NRAW;
-    unsigned char* dst = kv ? rawv(b) : rawk(b);
-    const uint32_t fb = bar((kv ? B_RVF : B_RKF) + b);
-    const unsigned char* src = (const unsigned char*)(kv ? p.v : p.k);
+    unsigned char* dst = rawv(b);
+    const uint32_t fb = bar(B_RVF + b);
+    const unsigned char* src = (const unsigned char*)p.v;
     int blk[kTT / kPage];
     if (PAGED) tile_blocks(t0, nload / kPage, blk);
     mbar_arrive_expect_tx(fb, (uint32_t)(nload * C::RB));
@@ -343,8 +346,6 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
     err_s = 0;
     abort_s = 0;
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(B_RKF + b), 1);
-      mbar_init(bar(B_RKE + b), kRoleWarps);
       mbar_init(bar(B_RVF + b), 1);
       mbar_init(bar(B_RVE + b), kRoleWarps);
       mbar_init(bar(B_KSF + b), kRoleWarps);
@@ -352,21 +353,20 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
       mbar_init(bar(B_STF + b), 1);
       mbar_init(bar(B_STE + b), kRoleWarps);
       mbar_init(bar(B_VF + b), kRoleWarps);
+      mbar_init(bar(B_PF + b), kRoleWarps);
+      mbar_init(bar(B_PE + b), 1);
       mbar_init(bar(B_VE + b), 1);
       mbar_init(bar(B_DRAIN + b), 1);
     }
-    mbar_init(bar(B_PF), kRoleWarps);
-    mbar_init(bar(B_PE), 1);
     mbar_init(bar(B_OF), 1);
     fence_barrier_init();
     if (early) {
+      // K rows go straight from L2 to the K dequantisation warps: bring
+      // the first tiles of K into L2 and V tile 0 into shared memory.
       const uint64_t pol = policy_evict_first();
-      issue(0, 0, pol);
-      issue(0, 1, pol);
-      for (int i = 1; i <= kPrefetch; ++i) {
-        prefetch(i, 0);
-        prefetch(i, 1);
-      }
+      for (int i = 0; i <= kPrefetch; ++i) prefetch(i, 0);
+      issue_v(0, pol);
+      for (int i = 1; i <= kPrefetch; ++i) prefetch(i, 1);
     }
   }
 
@@ -416,8 +416,11 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
       if (r < kNR) {
         *reinterpret_cast<uint4*>(qt + (chunk / 8) * C::QT_BLK + sw128(r, chunk % 8)) =
             make_uint4(h[0], h[1], h[2], h[3]);
-        if (chunk == 0) cm_s[r] = r < Rb ? make_float2(ldexpf(p.scale_log2, e), INFINITY)
-                                         : make_float2(0.f, INFINITY);
+        if (chunk == 0) {
+          const float c = ldexpf(p.scale_log2, e);
+          cm_s[r] = r < Rb ? make_float2(c, INFINITY) : make_float2(0.f, INFINITY);
+          rc_s[r] = r < Rb ? 1.f / c : 0.f;
+        }
       }
     }
     // Row tables (row r of the CTA = sequence-local query row rb*kNR + r).
@@ -468,7 +471,6 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
       // Let the copies already issued land before the CTA goes away.
       int dummy = 0;
       volatile int* never = &dummy;
-      mbar_wait(bar(B_RKF), 0, never, kWaitNs);
       mbar_wait(bar(B_RVF), 0, never, kWaitNs);
     }
     if (err && tid == 0) flag(p.status, err);
@@ -501,38 +503,32 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
   // warp of a warpgroup executes the same setmaxnreg).
   if (warp < W_SM0) {
    set_regs<REG_CTRL>();
-   if (warp == W_PROD) {
+   if (warp == W_PRODV) {
     // ------------------------------------------------------------ producer
+    // The V tiles into the raw buffer once the V dequantisation warps have
+    // read the buffer's last tile; K and V kPrefetch tiles ahead in L2 (the
+    // K dequantisation warps read K rows from L2 themselves).
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int ik = early ? 1 : 0, iv = ik;  // tiles issued per tensor
+      int issued = early ? 1 : 0;
       bool ok = true;
-      for (int i = ik; i < ntiles && ok; ++i) {
+      if (!early)
+        for (int i = 0; i <= kPrefetch; ++i) prefetch(i, 0);
+      for (int i = issued; i < ntiles && ok; ++i) {
         const int b = i % C::NRAW;
-        const uint32_t par = ((i / C::NRAW) & 1) ^ 1;
-        ok = mbar_wait(bar(B_RKE + b), par, abort_p, kWaitNs);
-        if (ok) {
-          issue(i, 0, pol);
-          ik = i + 1;
-        }
-        ok = ok && mbar_wait(bar(B_RVE + b), par, abort_p, kWaitNs);
-        if (ok) {
-          issue(i, 1, pol);
-          iv = i + 1;
-          // Keep both tensors kPrefetch tiles ahead in L2 (tiles 1.. as soon
-          // as tile 0 is out).
-          for (int j = (i == 0 ? 1 : i + kPrefetch); j <= i + kPrefetch; ++j) {
-            prefetch(j, 0);
-            prefetch(j, 1);
-          }
+        ok = mbar_wait(bar(B_RVE + b), ((i / C::NRAW) & 1) ^ 1, abort_p, kWaitNs);
+        if (!ok) break;
+        issue_v(i, pol);
+        issued = i + 1;
+        for (int j = (i == 0 ? 1 : i + kPrefetch); j <= i + kPrefetch; ++j) {
+          if (i > 0) prefetch(j, 0);
+          prefetch(j, 1);
         }
       }
       if (!ok) fail();
       if (*abort_p) {
         // Make sure no copy of ours is still landing in shared memory.
-        for (int i = max(0, ik - C::NRAW); i < ik; ++i)
-          mbar_wait(bar(B_RKF + i % C::NRAW), (i / C::NRAW) & 1, never, kWaitNs);
-        for (int i = max(0, iv - C::NRAW); i < iv; ++i)
+        for (int i = max(0, issued - C::NRAW); i < issued; ++i)
           mbar_wait(bar(B_RVF + i % C::NRAW), (i / C::NRAW) & 1, never, kWaitNs);
       }
     }
@@ -581,16 +577,16 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
     // steps of 16 tokens.  Completion frees P^T and the V buffer.
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, NR, false, true, true);
-      const uint32_t pt_a = smem_u32(pt);
       bool ok = true, any = false;
       for (int i = 0; i < ntiles && ok; ++i) {
         const int vb = i % C::NVB;
-        ok = mbar_wait(bar(B_PF), i & 1, abort_p, kWaitNs) &&
+        const int pb = i & 1;
+        ok = mbar_wait(bar(B_PF + pb), (i >> 1) & 1, abort_p, kWaitNs) &&
              mbar_wait(bar(B_VF + vb), (i / C::NVB) & 1, abort_p, kWaitNs);
         if (!ok) break;
         tc_fence_after();
         const uint32_t vt_a = smem_u32(vt(vb));
-        const uint64_t bd0 = sdesc_sw128(pt_a, C::PT_BLK, 1024);
+        const uint64_t bd0 = sdesc_sw128(smem_u32(ptb(pb)), C::PT_BLK, 1024);
 #pragma unroll
         for (int h = 0; h < C::DH; ++h) {
           const uint64_t ad0 = sdesc_sw128(vt_a + 2 * h * C::VT_BLK, C::VT_BLK, 1024);
@@ -602,7 +598,7 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
           }
         }
         any = true;
-        mma_commit(bar(B_PE));
+        mma_commit(bar(B_PE + pb));
         mma_commit(bar(B_VE + vb));
       }
       if (ok) mma_commit(bar(B_OF));
@@ -632,7 +628,8 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
     // named barriers as the other softmax warps, so a failing warp keeps
     // arriving there (skipping the work) until the loop ends.
     for (int i = 0; i < ntiles; ++i) {
-      const int b = i & 1;
+      const int b = i & 1;                     // S^T buffer and P^T buffer of this tile
+      unsigned char* const pt = ptb(b);
       if (ok && !__all_sync(0xffffffffu, mbar_wait(bar(B_STF + b), (i >> 1) & 1, abort_p, kWaitNs)))
         ok = false;
       tc_fence_after();
@@ -656,6 +653,26 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
           if (r < Rb && !draft_visible(kind, anc_s[r], jr_s[r], a)) su[r] = 0xFF800000u;  // -inf
       };
       if (cls == 1) mask_draft();
+      if (i == 0) {
+        // Seed each row's running maximum with the chunk's first token
+        // (thread t = 0; it lies inside the chunk, and a draft row that may
+        // not see it has its score masked to -inf): typical scores then stay
+        // within 2^kSlack of the seed and the first tile needs no rescale.
+        if (t == 0) {
+#pragma unroll
+          for (int r = 0; r < kNR; r += 4)
+            *reinterpret_cast<float4*>(&f_s[r]) = make_float4(SV(r), SV(r + 1), SV(r + 2), SV(r + 3));
+        }
+        bar_sync(1, 128);
+        if (t < Rb && ok) {
+          const float x = f_s[t] * cm_s[t].x;
+          const bool vis = x != -INFINITY;
+          m_s[t] = vis ? x : -INFINITY;
+          cm_s[t].y = vis ? x : INFINITY;
+          thr_s[t] = vis ? (x + kSlack) * rc_s[t] : -INFINITY;
+        }
+        bar_sync(1, 128);
+      }
       // Pass 1: does any visible score pass its row's trigger?
       bool hit = false;
       if (ok && cls != 2) {
@@ -671,15 +688,18 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
       const bool need = (flag_s[i & 1][0] | flag_s[i & 1][1] | flag_s[i & 1][2] | flag_s[i & 1][3]) != 0u;
       bool pe_done = false;
       if (need) {
-        // Some row's maximum moves.  The P^T buffer is free once the previous
-        // tile's P.V has landed; it holds bf16(s*c) of every (token, row)
-        // (-inf where not visible) while each owner thread r takes its row's
-        // maximum over the 128 tokens.
+        // Some row's maximum moves by more than 2^8 (or has not been set).
+        // The previous tile's P.V must have landed (it also releases this
+        // tile's P^T buffer, used as scratch here, and O^T for the rescale).
         if (i > 0) {
-          if (ok && !__all_sync(0xffffffffu, mbar_wait(bar(B_PE), (i - 1) & 1, abort_p, kWaitNs)))
+          if (ok && !__all_sync(0xffffffffu, mbar_wait(bar(B_PE + ((i - 1) & 1)), ((i - 1) >> 1) & 1,
+                                                       abort_p, kWaitNs)))
             ok = false;
           pe_done = true;
         }
+        // The P^T buffer (free now) holds bf16(s*c) of every (token, row),
+        // -inf where not visible; each owner thread r then takes its row's
+        // maximum over the 128 tokens.
 #pragma unroll
         for (int r = 0; r < kNR; r += 8) {
           uint32_t pk[4];
@@ -697,21 +717,28 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
         bar_sync(1, 128);
         if (t < Rb) {
           const int r = t;
-          const unsigned char* col = pt + (r >> 6) * C::PT_BLK + (((r & 63) & 7) << 1);
-          float M = -INFINITY;
-#pragma unroll 4
-          for (int tk = 0; tk < kTT; ++tk) {
-            const unsigned short bits =
-                *reinterpret_cast<const unsigned short*>(col + sw128(tk, (r & 63) >> 3));
-            M = fmaxf(M, __uint_as_float((uint32_t)bits << 16));
+          const unsigned char* col = pt + (r >> 6) * C::PT_BLK + ((r & 7) << 1);
+          float Mk[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) Mk[k] = -INFINITY;
+#pragma unroll 2
+          for (int tk = 0; tk < kTT; tk += 8) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const unsigned short bits =
+                  *reinterpret_cast<const unsigned short*>(col + sw128(tk + k, (r & 63) >> 3));
+              Mk[k] = fmaxf(Mk[k], __uint_as_float((uint32_t)bits << 16));
+            }
           }
+          const float M = fmaxf(fmaxf(fmaxf(Mk[0], Mk[1]), fmaxf(Mk[2], Mk[3])),
+                                fmaxf(fmaxf(Mk[4], Mk[5]), fmaxf(Mk[6], Mk[7])));
           const float m_old = m_s[r];
-          const bool upd = M != -INFINITY && (m_old == -INFINITY || M > m_old + 8.f);
+          const bool upd = M != -INFINITY && (m_old == -INFINITY || M > m_old + kSlack);
           const float m_new = upd ? M : m_old;
           const float f = upd ? (m_old == -INFINITY ? 0.f : ex2_approx(m_old - m_new)) : 1.f;
           m_s[r] = m_new;
           cm_s[r].y = m_new == -INFINITY ? INFINITY : m_new;
-          thr_s[r] = m_new == -INFINITY ? -INFINITY : (m_new + 8.f) / cm_s[r].x;
+          thr_s[r] = m_new == -INFINITY ? -INFINITY : (m_new + kSlack) * rc_s[r];
           f_s[r] = f;
         }
         bar_sync(1, 128);
@@ -726,23 +753,25 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
         if (i > 0 && ok) {
           // O^T columns of every row, this quadrant's lanes (values of d).
           tc_fence_after();
-          for (int h = 0; h < C::DH; ++h) {
 #pragma unroll 1
-            for (int c = 0; c < nch; ++c) {
-              const uint32_t oc = tm + lane_base + COL_O + h * kNR + 16 * c;
-              uint32_t o[16];
-              tmem_ld16(oc, o);
-              tmem_wait_ld();
+          for (int h = 0; h < C::DH; ++h) {
+            const uint32_t oc = tm + lane_base + COL_O + h * kNR;
+            uint32_t ou[kNR];
+            tmem_ld32_into<0>(oc, ou);
+            tmem_ld32_into<32>(oc + 32, ou);
+            tmem_ld32_into<64>(oc + 64, ou);
+            tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 16; j += 4) {
-                const float4 f4 = *reinterpret_cast<const float4*>(&f_s[16 * c + j]);
-                o[j] = __float_as_uint(__uint_as_float(o[j]) * f4.x);
-                o[j + 1] = __float_as_uint(__uint_as_float(o[j + 1]) * f4.y);
-                o[j + 2] = __float_as_uint(__uint_as_float(o[j + 2]) * f4.z);
-                o[j + 3] = __float_as_uint(__uint_as_float(o[j + 3]) * f4.w);
-              }
-              tmem_st16(oc, o);
+            for (int r = 0; r < kNR; r += 4) {
+              const float4 f4 = *reinterpret_cast<const float4*>(&f_s[r]);
+              ou[r] = __float_as_uint(__uint_as_float(ou[r]) * f4.x);
+              ou[r + 1] = __float_as_uint(__uint_as_float(ou[r + 1]) * f4.y);
+              ou[r + 2] = __float_as_uint(__uint_as_float(ou[r + 2]) * f4.z);
+              ou[r + 3] = __float_as_uint(__uint_as_float(ou[r + 3]) * f4.w);
             }
+            tmem_st32_from<0>(oc, ou);
+            tmem_st32_from<32>(oc + 32, ou);
+            tmem_st32_from<64>(oc + 64, ou);
           }
           tmem_wait_st();
         }
@@ -754,12 +783,15 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
           tmem_ld32_into<64>(scol + 64, su);
           tmem_wait_ld();
           if (cls == 1) mask_draft();
+        } else {
+#pragma unroll
+          for (int r = 0; r < kNR; ++r) su[r] = 0u;
         }
       }
-      // Pass 2: P = 2^(s c - m) into P^T (fp16), row sums in fp32, once the
-      // previous tile's P.V has read P^T.
-      if (i > 0 && !pe_done && ok &&
-          !__all_sync(0xffffffffu, mbar_wait(bar(B_PE), (i - 1) & 1, abort_p, kWaitNs)))
+      // Pass 2: P = 2^(s c - m) into this tile's P^T buffer (fp16), row sums
+      // in fp32, once the P.V of two tiles back has read that buffer.
+      if (i > 1 && !pe_done && ok &&
+          !__all_sync(0xffffffffu, mbar_wait(bar(B_PE + b), ((i >> 1) & 1) ^ 1, abort_p, kWaitNs)))
         ok = false;
       if (ok) {
         const float kill = cls == 2 ? -INFINITY : 0.f;
@@ -785,7 +817,7 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(bar(B_STE + b));
-        mbar_arrive(bar(B_PF));
+        mbar_arrive(bar(B_PF + b));
       }
     }
     // Epilogue: the last P.V; each row's sum over the 128 tokens in token
@@ -794,129 +826,125 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
     if (ok && !__all_sync(0xffffffffu, mbar_wait(bar(B_OF), 0, abort_p, kWaitNs))) ok = false;
     if (!ok && lane == 0) fail();
     tc_fence_after();
+    // Shared memory is idle now: the row sums go to the Q^T / P^T area, O^T
+    // to the V tile and raw-row area.
     constexpr int LP = kNR + 4;  // pitch (floats) of the [token][row] row sums
-    static_assert(kTT * LP * 4 <= 2 * C::VT_BLK * (C::NVB * C::DV / 128), "row-sum scratch");
-    float* lbuf = reinterpret_cast<float*>(vt(0));
+    constexpr int LBUF = kTT * LP * 4, OSTAGE = kNR * D * 4;
+    constexpr bool LOW = LBUF <= C::OFF_VT;  // row sums below the V tiles, else after O
+    static_assert(OSTAGE + (LOW ? 0 : LBUF) <= C::SMEM - 1024 - C::OFF_VT, "epilogue scratch");
+    float* lbuf = reinterpret_cast<float*>(LOW ? sm : vt(0) + OSTAGE);
 #pragma unroll
     for (int r = 0; r < kNR; r += 4)
       *reinterpret_cast<float4*>(lbuf + t * LP + r) = make_float4(l[r], l[r + 1], l[r + 2], l[r + 3]);
     bar_sync(1, 128);
     const bool bad = __any_sync(0xffffffffu, *abort_p != 0);
     if (t < Rb) {
-      float lt = 0.f;
-#pragma unroll 8
-      for (int tk = 0; tk < kTT; ++tk) lt += lbuf[tk * LP + t];
+      // Eight partial sums over tokens k, k + 8, ... then added in a fixed
+      // order: the row's sum depends only on its own values.
+      float ls[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+#pragma unroll 2
+      for (int tk = 0; tk < kTT; tk += 8) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ls[k] += lbuf[(tk + k) * LP + t];
+      }
+      const float lt = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       const long long si = slot_s[t];
       p.ws_ml[2 * si] = bad ? NAN : m_s[t];
       p.ws_ml[2 * si + 1] = bad ? NAN : lt;
     }
     if (!bad) {
+      // O^T half by half (every row's column in one TMEM round trip) into
+      // [row][d] fp32 rows in shared memory (lanes = consecutive d), then
+      // one bulk copy per row to its partial slot.
+      float* ostage = reinterpret_cast<float*>(vt(0));
+#pragma unroll 1
       for (int h = 0; h < C::DH; ++h) {
         const int d = 128 * h + 32 * quad + lane;
-#pragma unroll 1
-        for (int c = 0; c < nch; ++c) {
-          uint32_t o[16];
-          tmem_ld16(tm + lane_base + COL_O + h * kNR + 16 * c, o);
-          tmem_wait_ld();
-          if (d < D) {
+        const uint32_t oc = tm + lane_base + COL_O + h * kNR;
+        uint32_t ou[kNR];
+        tmem_ld32_into<0>(oc, ou);
+        tmem_ld32_into<32>(oc + 32, ou);
+        tmem_ld32_into<64>(oc + 64, ou);
+        tmem_wait_ld();
+        if (d < D) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int r = 16 * c + j;
-              if (r < Rb) p.ws_acc[slot_s[r] * D + d] = __uint_as_float(o[j]);
-            }
-          }
+          for (int r = 0; r < kNR; ++r)
+            if (r < Rb) ostage[r * D + d] = __uint_as_float(ou[r]);
         }
+      }
+      fence_proxy_async_smem();
+      bar_sync(1, 128);
+      if (t < Rb) {
+        bulk_s2g(p.ws_acc + slot_s[t] * D, smem_u32(ostage + t * D), (uint32_t)(D * 4));
+        bulk_commit_wait_all();
       }
     }
 #undef SV
   } else if (warp < W_VDQ0) {
     // ------------------------------------------------------------ K dequant
-    // Thread = token t of the tile (its TMEM lane).  A tile's raw row is
-    // taken in parts of up to four Q8 blocks (128 values of d); each part
-    // gives one or two K slot fills of 64 values: the hi and lo fp16 parts
-    // into the slot's two 32-column halves.  The raw buffer is released
-    // once the last part has been read.
+    // Thread = token t of the tile (its TMEM lane).  Per tile: the token's
+    // raw K row straight from L2 into registers (the producer keeps K tiles
+    // ahead in L2), then per K slot fill (64 values of d) the hi and lo fp16
+    // parts into the slot's two 32-column halves.
     set_regs<REG_KDQ>();
     const int quad = warp & 3;
     const int t = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const unsigned char* ksrc = reinterpret_cast<const unsigned char*>(p.k);
     const unsigned char* dsrc = reinterpret_cast<const unsigned char*>(p.dk);
-    constexpr int BPP = C::NB < 4 ? C::NB : 4;   // Q8 blocks per part
-    constexpr int PARTS = C::NB / BPP;
-    constexpr int PW = BPP * 34 / 4;              // words per part
-    constexpr int FPP = BPP / 2;                  // slot fills per part
     bool ok = true;
     int g = 0;
     for (int i = 0; i < ntiles && ok; ++i) {
-      const int b = i % C::NRAW;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_RKF + b), (i / C::NRAW) & 1, abort_p, kWaitNs))) {
-        ok = false;
-        break;
-      }
       const int tp = slo + i * kTT + t;
       const bool live = tp < shi;
-      const unsigned char* row = (scratch && tp >= ctx)
-                                     ? dsrc + scratch_row(p, row0, kvh, tp - ctx) * C::RB
-                                     : rawk(b) + t * C::RB;
-#pragma unroll 1
-      for (int part = 0; part < PARTS && ok; ++part) {
-        uint32_t w[PW + 1];
-        w[PW] = 0u;
-        if (live) {
-          const unsigned char* src = row + part * (BPP * 34);
-          if ((BPP * 34) % 8 == 0 && C::RB % 8 == 0) {
-#pragma unroll
-            for (int k = 0; k < PW / 2; ++k) {
-              const uint2 v = reinterpret_cast<const uint2*>(src)[k];
-              w[2 * k] = v.x;
-              w[2 * k + 1] = v.y;
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < PW; ++k) w[k] = reinterpret_cast<const uint32_t*>(src)[k];
-          }
+      uint32_t w[C::NW + 1];
+      w[C::NW] = 0u;
+      if (live) {
+        const unsigned char* src;
+        if (scratch && tp >= ctx) {
+          src = dsrc + scratch_row(p, row0, kvh, tp - ctx) * C::RB;
+        } else if (!PAGED) {
+          src = ksrc + (((long long)s * p.KVH + kvh) * p.capacity + tp) * C::RB;
+        } else {
+          const int blk = p.block_table[(long long)s * p.max_blocks + tp / kPage];
+          src = ksrc + (((long long)blk * p.KVH + kvh) * kPage + tp % kPage) * C::RB;
         }
-        if (part == PARTS - 1) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_RKE + b));
-        }
-#pragma unroll
-        for (int fp = 0; fp < FPP; ++fp, ++g) {
-          const int ks = g & 1;
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_KSE + ks), ((g >> 1) & 1) ^ 1, abort_p, kWaitNs))) {
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            uint32_t hv[16], lv[16];
-            if (live) {
-              __half2 d2;
-              uint32_t code[8];
-              q8_block(w, 2 * fp + hb, d2, code);
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                __half2 x0, x1;
-                codes_to_h2(code[q], x0, x1);
-                const __half2 h0 = __hmul2(x0, d2), h1 = __hmul2(x1, d2);
-                hv[2 * q] = h2u(h0);
-                hv[2 * q + 1] = h2u(h1);
-                lv[2 * q] = h2u(__hfma2(x0, d2, __hneg2(h0)));
-                lv[2 * q + 1] = h2u(__hfma2(x1, d2, __hneg2(h1)));
-              }
-            } else {
-#pragma unroll
-              for (int q = 0; q < 16; ++q) hv[q] = lv[q] = 0u;
-            }
-            tmem_st16(tm + lane_base + COL_K + ks * 64 + hb * 16, hv);
-            tmem_st16(tm + lane_base + COL_K + ks * 64 + 32 + hb * 16, lv);
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_KSF + ks));
-        }
+        load_row<D>(*reinterpret_cast<uint32_t(*)[C::NW]>(w), src);
       }
+#pragma unroll
+      for (int f = 0; f < C::NFILL; ++f) {
+        const int ks = (g + f) & 1;
+        if (ok && !__all_sync(0xffffffffu, mbar_wait(bar(B_KSE + ks), (((g + f) >> 1) & 1) ^ 1,
+                                                     abort_p, kWaitNs)))
+          ok = false;
+        if (!ok) continue;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t hv[16], lv[16];
+          __half2 d2;
+          uint32_t code[8];
+          q8_block(w, 2 * f + hb, d2, code);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            __half2 x0, x1;
+            codes_to_h2(code[q], x0, x1);
+            const __half2 h0 = __hmul2(x0, d2), h1 = __hmul2(x1, d2);
+            hv[2 * q] = live ? h2u(h0) : 0u;
+            hv[2 * q + 1] = live ? h2u(h1) : 0u;
+            lv[2 * q] = live ? h2u(__hfma2(x0, d2, __hneg2(h0))) : 0u;
+            lv[2 * q + 1] = live ? h2u(__hfma2(x1, d2, __hneg2(h1))) : 0u;
+          }
+          tmem_st16(tm + lane_base + COL_K + ks * 64 + hb * 16, hv);
+          tmem_st16(tm + lane_base + COL_K + ks * 64 + 32 + hb * 16, lv);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_KSF + ks));
+      }
+      g += C::NFILL;
     }
     if (!ok && lane == 0) fail();
   } else {
@@ -954,29 +982,22 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
         unsigned char* col = dst + pr * C::VT_BLK;
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
-          uint4 out[4];
-          if (live) {
-            __half2 d2;
-            uint32_t code[8];
-            q8_block(w, hb, d2, code);
-            uint32_t hv[16];
+          __half2 d2;
+          uint32_t code[8];
+          q8_block(w, hb, d2, code);
+          // 8 values of d (one 16-byte chunk) at a time.
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              __half2 x0, x1;
-              codes_to_h2(code[q], x0, x1);
-              hv[2 * q] = h2u(__hmul2(x0, d2));
-              hv[2 * q + 1] = h2u(__hmul2(x1, d2));
+          for (int c = 0; c < 4; ++c) {
+            uint4 out = make_uint4(0u, 0u, 0u, 0u);
+            if (live) {
+              __half2 x0, x1, x2, x3;
+              codes_to_h2(code[2 * c], x0, x1);
+              codes_to_h2(code[2 * c + 1], x2, x3);
+              out = make_uint4(h2u(__hmul2(x0, d2)), h2u(__hmul2(x1, d2)), h2u(__hmul2(x2, d2)),
+                               h2u(__hmul2(x3, d2)));
             }
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              out[c] = make_uint4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) out[c] = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(col + sw128(t, hb * 4 + c)) = out;
           }
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(col + sw128(t, hb * 4 + c)) = out[c];
         }
       }
       fence_proxy_async_smem();
