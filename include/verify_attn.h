@@ -31,10 +31,16 @@
  *   - Calls are asynchronous on the given CUDA stream (a cudaStream_t passed
  *     as void*; NULL = legacy default stream).  Lengths and metadata are read
  *     on the device, so the host never synchronises.
+ *   - The stream must belong to the current device (the plan uses that
+ *     device's SM count); outside stream capture, a stream of another
+ *     device returns VA_ERR_INVALID_ARG and launches nothing (a capturing
+ *     stream's device cannot be queried without ending the capture, so
+ *     there the caller's word stands).
  *   - Host-checkable errors return a status and launch nothing.
  *   - Data errors found on the device (bad parent, block id, row counts,
  *     context beyond capacity) OR a VA_DEV_* bit into *status (device word,
- *     may be NULL) and the affected rows get NaN outputs.
+ *     may be NULL) and the affected rows get NaN outputs (for inconsistent
+ *     row offsets, VA_DEV_BAD_ROWS, every row of that sequence).
  */
 #ifndef VERIFY_ATTN_H
 #define VERIFY_ATTN_H
@@ -95,9 +101,9 @@ typedef enum va_mode {
  *   for the context only (capacity, or block-table entries, for ctx_len[s]
  *   tokens).  Chain and direct sequences always read the cache: prefill and
  *   direct rows write durable KV, tree rows write scratch KV (lucebox PR
- *   #686, "State and commit invariants").  With a scratch KV the
- *   tensor-core kernel serves Q8_0 paged caches; other caches run on the
- *   CUDA-core kernel.
+ *   #686, "State and commit invariants").  With a scratch KV, Q8_0 caches
+ *   (contiguous or paged) run on the transposed tensor-core kernel and other
+ *   caches on the CUDA-core kernel.
  */
 typedef struct va_kv {
   va_dtype dtype;
@@ -251,6 +257,23 @@ va_status va_debug_gather_index(const va_problem *p, const va_kv *kv, int32_t kv
                                 int64_t max_len, int64_t *phys_row, uint32_t *status,
                                 void *stream);
 
+/*
+ * Debug export of the KV chunks the partial kernels run (the split plan of
+ * hipfire PR #817 "Summary": each sequence's span cut into chunks whose
+ * partials a merge combines; lucebox PR #686 "Correctness failure found
+ * during qualification": the cut must not depend on what else shares the
+ * launch).  For sequence s and slot j < T (T = va_plan's slots),
+ * ranges[2*(s*T + j)] and ranges[2*(s*T + j) + 1] are the first and
+ * one-past-last KV position of chunk j, computed by the device functions
+ * the partial kernels call: with L = ctx_len[s] + rows of s, a chunk has
+ * c = max(ceil(L / T), 128) rounded up to a multiple of 64 tokens and
+ * chunk j is [min(j c, L), min((j + 1) c, L)) (empty past L).  A sequence
+ * whose row offsets are inconsistent gets -1, -1 and sets
+ * VA_DEV_BAD_ROWS.  ranges: device int32[num_seqs * T * 2].
+ */
+va_status va_debug_split_ranges(const va_problem *p, const va_kv *kv, int32_t mode,
+                                int32_t *ranges, uint32_t *status, void *stream);
+
 /* Plan details for a problem (which kernel runs, splits and sub-splits). */
 /* Partial kernels (va_plan_info.kernel). */
 #define VA_KERNEL_CUDA_CORES 0 /* fp32 FMA, one thread block per 16 query rows */
@@ -284,9 +307,9 @@ va_status va_timing_read(int32_t max_calls, float *partial_ms, float *merge_ms,
 
 /*
  * Verify attention without a caller workspace and without any allocation
- * on the call path.  The pages have no counterpart: their split-KV route
- * takes a caller-owned workspace (hipfire PR #817 "Maintainer-review
- * follow-up"), which verify_attn_chain/tree/mixed keep.
+ * on the call path.  The pages have no counterpart to this entry point;
+ * verify_attn_chain/tree/mixed, which take a caller workspace, are the
+ * pages' route.
  *
  * For callers that cannot hand the library device memory per call: code
  * that owns no allocator (a plain C host program, a runtime whose device
@@ -307,6 +330,8 @@ va_status va_timing_read(int32_t max_calls, float *partial_ms, float *merge_ms,
  *     38 slots x 50 rows x 24 heads do not) return
  *     VA_ERR_WORKSPACE_TOO_SMALL before any launch; use the entry points
  *     with a caller workspace for those.
+ *   - The scratch used is the current device's, and the stream must belong
+ *     to that device (VA_ERR_INVALID_ARG otherwise, nothing launched).
  *   - The first call on each device looks the scratch address up with
  *     cudaGetSymbolAddress (VA_ERR_CUDA if that fails); make that first
  *     call, on every device it will be used on, outside any stream capture.

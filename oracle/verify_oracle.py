@@ -228,6 +228,30 @@ def split_ranges(L: int, S: int) -> list[tuple[int, int]]:
     return [(min(s * chunk, L), min((s + 1) * chunk, L)) for s in range(S)]
 
 
+def device_chunk_count(S: int, num_kv_heads: int, sm_count: int, ctas_per_sm: int) -> int:
+    """How many chunks (T) the GPU library cuts each sequence into: one wave
+    of CTAs per (sequence, KV head), i.e. ctas_per_sm * sm_count //
+    num_kv_heads, kept within [S, 16 S].  ctas_per_sm is 1 for the
+    tensor-core kernels and 2 for the CUDA-core kernel.  Not a rule of the
+    pages (they fix only that the cut follows the sequence's own span and
+    S): the library's reading of "S chunks", restated here so that tests can
+    pin the chunks its kernels run."""
+    T = ctas_per_sm * sm_count // num_kv_heads
+    return max(S, min(T, 16 * S))
+
+
+def device_chunk_ranges(L: int, T: int) -> list[tuple[int, int]]:
+    """The GPU library's chunks of a span of L tokens cut T ways: chunk
+    length c = max(ceil(L / T), 128) rounded up to a multiple of 64 tokens
+    (whole 64-token tiles, at least two of them), chunk j = [min(j c, L),
+    min((j + 1) c, L)); trailing chunks may be empty.  Like split_ranges it
+    depends on the sequence's own span only (lucebox PR #686, "Correctness
+    failure found during qualification")."""
+    c = max(-(-L // T), 128)
+    c = -(-c // 64) * 64
+    return [(min(j * c, L), min((j + 1) * c, L)) for j in range(T)]
+
+
 def partial(q, K, V, pos, lo: int, hi: int, scale: float):
     """Online-softmax partial of one chunk: (m, l, acc) over the visible
     positions inside [lo, hi); an empty chunk gives (-inf, 0, 0)."""

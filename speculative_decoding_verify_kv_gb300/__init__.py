@@ -41,7 +41,7 @@ MODE_CODES = {"chain": MODE_CHAIN, "tree": MODE_TREE, "mixed": MODE_MIXED}
 EXPORTED = ["va_version", "va_status_string", "va_last_cuda_error", "va_workspace_size", "va_validate",
             "verify_attn_chain", "verify_attn_tree", "verify_attn_mixed",
             "va_debug_row_map", "va_debug_gather_index", "va_plan", "va_timing_enable",
-            "va_timing_read", "verify_attn_noalloc", "verify_attn_promote"]
+            "va_timing_read", "verify_attn_noalloc", "verify_attn_promote", "va_debug_split_ranges"]
 
 
 class VaKV(ctypes.Structure):
@@ -99,6 +99,9 @@ def _load():
                                           ctypes.c_void_p]
     lib.va_plan.restype = ctypes.c_int
     lib.va_plan.argtypes = [P(VaProblem), P(VaKV), ctypes.c_int32, P(VaPlanInfo)]
+    lib.va_debug_split_ranges.restype = ctypes.c_int
+    lib.va_debug_split_ranges.argtypes = [P(VaProblem), P(VaKV), ctypes.c_int32, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p]
     lib.va_timing_enable.restype = ctypes.c_int
     lib.va_timing_enable.argtypes = [ctypes.c_int32]
     lib.verify_attn_noalloc.restype = ctypes.c_int
@@ -301,6 +304,19 @@ def debug_gather_index(p: Problem, kv: KV, kv_head: int, max_len: int, status=No
     if st:
         raise VaError(st, "va_debug_gather_index")
     return out
+
+
+def debug_split_ranges(p: Problem, kv: KV, mode: int = MODE_CHAIN, status=None, stream=None):
+    """Each sequence's KV chunks as the partial kernels cut them: an int32
+    tensor [num_seqs][slots][2] of (lo, hi) positions."""
+    import torch
+    slots = plan(p, kv, mode)["slots"]
+    out = torch.full((max(p.num_seqs, 1), slots, 2), -2, dtype=torch.int32, device=p.cu_rows.device)
+    st = lib.va_debug_split_ranges(ctypes.byref(p.c()), ctypes.byref(kv.c()), mode, _ptr(out),
+                                   _ptr(status), _stream_handle(stream))
+    if st:
+        raise VaError(st, "va_debug_split_ranges")
+    return out[:p.num_seqs]
 
 
 def upload(case, device="cuda", num_splits=None, flags: int = 0):

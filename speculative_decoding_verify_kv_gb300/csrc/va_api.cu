@@ -33,6 +33,7 @@ static va_status note_cuda(cudaError_t e) {
 }
 cudaError_t launch_merge(const Params& p, cudaStream_t st);
 cudaError_t launch_debug_row_map(const Params& p, int* row_seq, unsigned* anc, cudaStream_t st);
+cudaError_t launch_debug_split(const Params& p, int* ranges, cudaStream_t st);
 cudaError_t launch_promote(const Params& p, const int* acc_len, const int* nodes,
                            cudaStream_t st);
 cudaError_t launch_debug_gather(const Params& p, int kvh, long long max_len, long long* out,
@@ -54,6 +55,25 @@ static int sm_count() {
 }
 
 static bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
+
+// The plan (the SM count) and the library-held scratch are the current
+// device's, so a stream must belong to the current device; the default
+// streams always do.  Checked outside stream capture only: querying a
+// capturing stream's device is not a capturable operation and would
+// invalidate the capture.
+static va_status check_stream_device(cudaStream_t s) {
+  if (s == nullptr || s == cudaStreamLegacy || s == cudaStreamPerThread) return VA_OK;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cap);
+  if (e != cudaSuccess) return note_cuda(e);
+  if (cap != cudaStreamCaptureStatusNone) return VA_OK;
+  int dev = 0, sdev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return note_cuda(e);
+  e = cudaStreamGetDevice(s, &sdev);
+  if (e != cudaSuccess) return note_cuda(e);
+  return sdev == dev ? VA_OK : VA_ERR_INVALID_ARG;
+}
 
 static int row_bytes_of(int dtype, int D) {
   switch (dtype) {
@@ -269,8 +289,10 @@ static va_status run(const va_problem* p, const va_kv* kv, int mode, void* ws, s
   size_t need = ws_bytes_for(p, kv, pl);
   if (!ws || ws_bytes < need) return VA_ERR_WORKSPACE_TOO_SMALL;
   if (((uintptr_t)ws & 255u) != 0) return VA_ERR_ALIGNMENT;
-  Params q = make_params(p, kv, mode, pl, ws, o, lse, status);
   cudaStream_t cs = (cudaStream_t)stream;
+  st = check_stream_device(cs);
+  if (st != VA_OK) return st;
+  Params q = make_params(p, kv, mode, pl, ws, o, lse, status);
   TimingSlot* ts = timing_slot();
   // External records so that, under stream capture, they become event
   // nodes of the graph (plain records only order work inside a capture).
@@ -417,6 +439,18 @@ va_status va_debug_gather_index(const va_problem* p, const va_kv* kv, int32_t kv
   return e == cudaSuccess ? VA_OK : note_cuda(e);
 }
 
+va_status va_debug_split_ranges(const va_problem* p, const va_kv* kv, int32_t mode,
+                                int32_t* ranges, uint32_t* status, void* stream) {
+  va_status st = check(p, kv, mode);
+  if (st != VA_OK) return st;
+  if (!ranges) return VA_ERR_INVALID_ARG;
+  if (p->num_seqs == 0) return VA_OK;
+  Plan pl = make_plan(p, kv);
+  Params q = make_params(p, kv, mode, pl, nullptr, nullptr, nullptr, status);
+  cudaError_t e = launch_debug_split(q, (int*)ranges, (cudaStream_t)stream);
+  return e == cudaSuccess ? VA_OK : note_cuda(e);
+}
+
 va_status verify_attn_promote(const va_problem* p, const va_kv* kv, int32_t mode,
                               const int32_t* accepted_len, const int32_t* accepted_nodes,
                               uint32_t* status, void* stream) {
@@ -483,11 +517,13 @@ va_status verify_attn_noalloc(const va_problem* p, const va_kv* kv, int32_t mode
   Plan pl = make_plan(p, kv);
   if (ws_bytes_for(p, kv, pl) > (size_t)VA_STATIC_WORKSPACE_BYTES)
     return VA_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t cs = (cudaStream_t)stream;
+  st = check_stream_device(cs);
+  if (st != VA_OK) return st;
   void* ws = nullptr;
   cudaError_t e = static_workspace(&ws);
   if (e != cudaSuccess) return note_cuda(e);
   Params q = make_params(p, kv, mode, pl, ws, o, lse, status);
-  cudaStream_t cs = (cudaStream_t)stream;
   e = launch_partial(pl, q, cs);
   if (e != cudaSuccess) return note_cuda(e);
   e = launch_merge(q, cs);

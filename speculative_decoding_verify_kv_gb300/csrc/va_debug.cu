@@ -41,6 +41,30 @@ __global__ void debug_gather_kernel(const Params p, int kvh, long long max_len, 
   out[(long long)s * max_len + t] = v;
 }
 
+// One block per sequence, its threads striding over the slots: each
+// chunk's [lo, hi) exactly as the partial kernels compute it.
+__global__ void debug_split_kernel(const Params p, int* ranges) {
+  const int s = blockIdx.x;
+  int row0, n, ctx;
+  const unsigned err = check_sequence(p, s, &row0, &n, &ctx);
+  for (int j = threadIdx.x; j < p.slots; j += blockDim.x) {
+    int slo = -1, shi = -1;
+    if (!(err & VA_DEV_BAD_ROWS)) {
+      int lo, hi;
+      split_range(ctx + n, p.S, 0, &lo, &hi);
+      sub_range(lo, hi, p.P, p.min_sub, j, &slo, &shi);
+    }
+    ranges[2 * ((long long)s * p.slots + j)] = slo;
+    ranges[2 * ((long long)s * p.slots + j) + 1] = shi;
+  }
+  if (threadIdx.x == 0 && (err & VA_DEV_BAD_ROWS)) flag(p.status, err & VA_DEV_BAD_ROWS);
+}
+
+cudaError_t launch_debug_split(const Params& p, int* ranges, cudaStream_t st) {
+  debug_split_kernel<<<p.num_seqs, 64, 0, st>>>(p, ranges);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_debug_row_map(const Params& p, int* row_seq, unsigned* anc, cudaStream_t st) {
   debug_row_map_kernel<<<p.num_seqs, 32, 0, st>>>(p, row_seq, anc);
   return cudaGetLastError();

@@ -5,7 +5,8 @@
 // * ln 2.  A slot with l = 0 is an empty chunk and is skipped; a NaN slot
 // (device-detected error) makes the row NaN.  The summation order is fixed
 // (slots of a group in ascending order, then groups in ascending order), so
-// a row's output depends only on its own slots.
+// a row's output depends only on its own slots.  Rows of a sequence whose
+// row range is inconsistent (VA_DEV_BAD_ROWS) are NaN.
 //
 // Restated from hipfire PR #817 "FA2 split-KV" sections "Summary" and
 // "Performance" (S8 partials combined by a merge pass; S1 equals the
@@ -47,8 +48,20 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const Params p)
   const int tcol = threadIdx.x % TC, grp = threadIdx.x / TC;
   float Mg = -INFINITY, lg = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  int nan = 0;
-  for (int s0 = grp; s0 < p.slots; s0 += BATCH * NG) {
+  // The row's sequence: the last s with cu_rows[s] <= row.  A row that no
+  // sequence covers, or whose sequence has inconsistent rows (the partial
+  // kernel flags VA_DEV_BAD_ROWS and writes none of its slots), comes out
+  // NaN, so that scratch left by an earlier call never reaches O.
+  int s_lo = 0, s_hi = p.num_seqs - 1;
+  while (s_lo < s_hi) {
+    const int mid = (s_lo + s_hi + 1) >> 1;
+    if (p.cu_rows[mid] <= grow) s_lo = mid;
+    else s_hi = mid - 1;
+  }
+  int sr0, sn, sctx;
+  int nan = !(p.cu_rows[s_lo] <= grow && grow < p.cu_rows[s_lo + 1]) ||
+            (check_sequence(p, s_lo, &sr0, &sn, &sctx) & VA_DEV_BAD_ROWS) != 0u;
+  for (int s0 = grp; s0 < p.slots && !nan; s0 += BATCH * NG) {
     float mm[BATCH], ll[BATCH];
     float4 aa[BATCH];
 #pragma unroll

@@ -44,14 +44,3 @@ def compare(o, lse, O, L, what=""):
     return max_abs, rel, lse_err
 
 
-def sample_rows_heads(case):
-    """Rows {first, middle, last} of each sequence and heads at the edges
-    of the first and last GQA groups."""
-    rows = set()
-    for s in range(case.num_seqs):
-        lo, hi = int(case.cu_rows[s]), int(case.cu_rows[s + 1])
-        if hi > lo:
-            rows |= {lo, (lo + hi - 1) // 2, hi - 1}
-    G = case.num_heads // case.num_kv_heads
-    heads = sorted({0, G - 1, G, case.num_heads - 1} & set(range(case.num_heads)))
-    return sorted(rows), heads

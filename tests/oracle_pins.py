@@ -118,6 +118,35 @@ def check_split_golden():
         assert got == c["ranges"], (c["L"], c["S"], got)
 
 
+def check_device_split_golden():
+    """The GPU library's chunk count and chunks against hand-worked cases."""
+    d = load("device_split_plan.json")
+    for c in d["cases"]:
+        T = orc.device_chunk_count(c["S"], c["KVH"], c["sms"], c["ctas_per_sm"])
+        assert T == c["T"], (c["work"], T)
+        want = [(j * c["c"], (j + 1) * c["c"]) for j in range(c["full"])]
+        if c["tail"] is not None:
+            want.append(tuple(c["tail"]))
+        want += [(c["L"], c["L"])] * c["empty"]
+        got = orc.device_chunk_ranges(c["L"], T)
+        assert got == want, (c["work"], got[:3], got[-3:])
+
+
+def check_device_split_properties():
+    """Chunks tile [0, L) in order; every chunk but the last non-empty one is
+    a whole number of 64-token tiles and at least 128 tokens."""
+    for L in [1, 63, 64, 127, 128, 129, 1000, 1024, 1032, 4097, 20676, 32784, 100000]:
+        for T in [1, 2, 8, 16, 37, 38, 76, 128]:
+            rs = orc.device_chunk_ranges(L, T)
+            assert len(rs) == T and rs[0][0] == 0 and rs[-1][1] == L
+            for (a, b), (c, _) in zip(rs, rs[1:]):
+                assert b == c and a <= b
+            live = [(a, b) for a, b in rs if b > a]
+            for a, b in live[:-1]:
+                assert (b - a) % 64 == 0 and b - a >= 128, (L, T, a, b)
+            assert live[-1][1] - live[-1][0] <= live[0][1] - live[0][0]
+
+
 def check_split_rule_properties():
     for L in [1, 2, 15, 16, 17, 255, 1024, 1025, 1032, 4097, 20676, 32784]:
         for S in [1, 2, 3, 5, 8, 13, 64]:

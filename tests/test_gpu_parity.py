@@ -10,7 +10,8 @@ import pytest
 
 import oracle
 import synthetic as sy
-from gpu_util import compare, run_gpu, sample_rows_heads
+from gpu_util import compare, run_gpu
+from oracle_parallel import oracle_full
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -260,13 +261,15 @@ def test_context_overflow_is_flagged():
 
 
 # --------------------------------------------------------------------------
-# The five verify workloads at full size, in the bench's launch configuration.
+# The five verify workloads at full size, in the bench's launch configuration,
+# every (row, head) against the oracle (run over the host's cores).
 
-def sampled(case, S, flags=0):
-    rows, heads = sample_rows_heads(case)
+def full_size(recipe, S, flags=0):
+    case = getattr(sy, recipe[0])(**recipe[1])
     o, lse = run_gpu(case, num_splits=S, flags=flags)
-    O, L = oracle.verify_case(case, rows=rows, heads=heads)
-    return compare(o, lse, O, L, f"{case.name} S={S} (sampled)")
+    O, L = oracle_full(recipe, case)
+    assert not np.isnan(L).any()
+    return compare(o, lse, O, L, f"{case.name} S={S} (every row and head)")
 
 
 @pytest.mark.parametrize("S", [1, 8])
@@ -276,30 +279,26 @@ def test_workload_dflash_bf16_ctx4096_full(S):
 
 @pytest.mark.parametrize("S", [1, 8])
 def test_workload_dflash_bf16_ctx8192(S):
-    sampled(sy.dflash_bf16(ctx=8192), S)
+    full_size(("dflash_bf16", {"ctx": 8192}), S)
 
 
 @pytest.mark.parametrize("ctx", [8192, 20676, 32768])
 def test_workload_long_q8(ctx):
-    sampled(sy.long_q8(ctx=ctx), 8)
+    full_size(("long_q8", {"ctx": ctx}), 8)
 
 
 def test_workload_paged_d128():
-    sampled(sy.paged_d128(), 8)
+    full_size(("paged_d128", {}), 8)
 
 
 def test_workload_paged_d128_q8():
     """The batched D=128 shape over a paged Q8_0 cache (the Q8 D=128 path)."""
-    c = sy.paged_d128(kv_dtype=sy.Q8_0)
-    rows, heads = sample_rows_heads(c)
-    o, lse = run_gpu(c, num_splits=8)
-    O, L = oracle.verify_case(c, rows=rows, heads=heads)
-    compare(o, lse, O, L, f"{c.name} S=8 (sampled)")
+    full_size(("paged_d128", {"kv_dtype": sy.Q8_0}), 8)
 
 
 def test_workload_mixed_tree_direct():
     c = sy.mixed_tree_direct()
-    sampled(c, 8)
+    full_size(("mixed_tree_direct", {}), 8)
     o, lse = _gpu(c, 8)
     d = sy.subset_sequences(c, [0, 1])
     od, ld = _gpu(d, 8)

@@ -11,7 +11,7 @@ import oracle_pins as P
     "check_golden_attention", "check_brute_force", "check_weights_sum_to_one",
     "check_closed_forms", "check_split_invariance", "check_chain_is_tree_with_chain_parents",
     "check_direct_rows_independent_of_launch", "check_tree_commit_golden",
-    "check_commit_then_chain",
+    "check_commit_then_chain", "check_device_split_golden", "check_device_split_properties",
 ])
 def test_pin(name):
     getattr(P, name)()
@@ -20,3 +20,18 @@ def test_pin(name):
 @pytest.mark.parametrize("S", [1, 2, 8])
 def test_golden_attention_split_route(S):
     P.check_golden_attention(num_splits=S)
+
+
+def test_parallel_oracle_equals_the_oracle():
+    """The row-parallel driver of the full-size tests only distributes rows:
+    its result is the oracle's, bit for bit."""
+    import numpy as np
+
+    import oracle
+    import synthetic as sy
+    from oracle_parallel import oracle_full
+    recipe = ("mixed_tree_direct", {"ctx": [40, 300, 17, 130, 64, 5, 90, 200]})
+    case = sy.mixed_tree_direct(ctx=recipe[1]["ctx"])
+    O, L = oracle_full(recipe, case)
+    O2, L2 = oracle.verify_case(case)
+    assert np.array_equal(O, O2) and np.array_equal(L, L2)

@@ -13,7 +13,7 @@ ALL_PINS = [
     P.check_split_golden, P.check_gather_golden, P.check_paged_equals_contiguous,
     P.check_golden_attention, P.check_brute_force, P.check_closed_forms,
     P.check_split_invariance, P.check_chain_is_tree_with_chain_parents,
-    P.check_tree_commit_golden, P.check_commit_then_chain,
+    P.check_tree_commit_golden, P.check_commit_then_chain, P.check_device_split_golden,
 ]
 
 
@@ -68,6 +68,21 @@ def _split_no_rounding(L, S):
     return [(min(s * chunk, L), min((s + 1) * chunk, L)) for s in range(S)]
 
 
+def _device_chunks_tile16(L, T):
+    c = max(-(-L // T), 128)
+    c = -(-c // 16) * 16
+    return [(min(j * c, L), min((j + 1) * c, L)) for j in range(T)]
+
+
+def _device_chunks_no_minimum(L, T):
+    c = -(-(-(-L // T)) // 64) * 64
+    return [(min(j * c, L), min((j + 1) * c, L)) for j in range(T)]
+
+
+def _device_count_unclamped(S, num_kv_heads, sm_count, ctas_per_sm):
+    return ctas_per_sm * sm_count // num_kv_heads
+
+
 def _merge_no_rescale(parts):
     live = [p for p in parts if p[1] > 0]
     M = max(p[0] for p in live)
@@ -119,7 +134,7 @@ def _span_rows_scratch_shifted(cache, draft, s, kvh, ctx, n, lo, **kw):
 _orig = {name: getattr(orc, name) for name in
          ["attend", "visible_positions", "ancestors", "kv_head_of", "dequant_q8_0",
           "decode_fp16", "split_ranges", "merge", "gather_index", "promote",
-          "promote_preflight", "span_rows"]}
+          "promote_preflight", "span_rows", "device_chunk_ranges", "device_chunk_count"]}
 
 MUTATIONS = {
     "scale dropped": ("attend", _attend_no_scale),
@@ -137,6 +152,9 @@ MUTATIONS = {
     "commit lands one position late": ("promote", _promote_one_late),
     "commit preflight ignores the tree": ("promote_preflight", _preflight_ignores_parents),
     "scratch rows off by one": ("span_rows", _span_rows_scratch_shifted),
+    "device chunks in 16-token steps": ("device_chunk_ranges", _device_chunks_tile16),
+    "device chunks without the 128-token minimum": ("device_chunk_ranges", _device_chunks_no_minimum),
+    "device chunk count not clamped to [S, 16 S]": ("device_chunk_count", _device_count_unclamped),
 }
 
 

@@ -13,7 +13,6 @@ import pytest
 
 import speculative_decoding_verify_kv_gb300 as va
 import synthetic as sy
-from gpu_util import LSE_MAX_ABS, O_MAX_ABS, O_REL_L2
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
                       "verify_attn.h")
@@ -75,7 +74,7 @@ def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row(name):
     o_ref, l_ref = va.verify_attn(p, kv, mode, status=st_ref)
     torch.cuda.synchronize()
     assert int(st_ref.item()) == 0
-    o_ref, l_ref = o_ref.cpu().numpy().astype(np.float64), l_ref.cpu().numpy().astype(np.float64)
+    o_ref, l_ref = o_ref.cpu().numpy(), l_ref.cpu().numpy()
 
     o = torch.empty((case.total_rows, case.num_heads, case.head_dim), dtype=torch.float32,
                     device="cuda")
@@ -90,13 +89,14 @@ def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row(name):
         torch.cuda.synchronize()
         free.append(torch.cuda.mem_get_info()[0])
         assert int(status.item()) == 0, f"call {call}: device status {int(status.item()):#x}"
-        go, gl = o.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+        go, gl = o.cpu().numpy(), lse.cpu().numpy()
         assert np.isfinite(go).all() and np.isfinite(gl).all(), f"call {call}: unwritten output"
-        d = go - o_ref
-        max_abs = float(np.abs(d).max())
-        rel = float(np.linalg.norm(d) / np.linalg.norm(o_ref))
-        lse_err = float(np.abs(gl - l_ref).max())
-        assert max_abs <= O_MAX_ABS and rel <= O_REL_L2 and lse_err <= LSE_MAX_ABS, (
-            f"call {call}: max|dO|={max_abs:.3e} relL2={rel:.3e} max|dLSE|={lse_err:.3e}")
+        # Same plan, same kernels, same arithmetic: only the scratch address
+        # differs, so the outputs are the same bits.
+        assert np.array_equal(go.view(np.uint32), o_ref.view(np.uint32)), (
+            f"call {call}: O differs from the workspace entry point in "
+            f"{int((go.view(np.uint32) != o_ref.view(np.uint32)).sum())} elements")
+        assert np.array_equal(gl.view(np.uint32), l_ref.view(np.uint32)), (
+            f"call {call}: LSE differs from the workspace entry point")
     # The second call allocated no device memory.
     assert free[1] == free[0]
