@@ -5,15 +5,18 @@ verify shape — 1 sequence, B=16 chain rows, H24/KV4/D256, Q8_0 cache, bf16
 Q, context 32,768, split-KV S=8 — on synthetic seeded inputs.  Contexts
 8,192 and 20,676 are measured too and reported under ``contexts``.
 
-Timing: W eager warm-up calls, then EXACTLY K calls replayed from CUDA
-graphs, bracketed by a barrier and cudaDeviceSynchronize, timed with CUDA
-events on the launching stream; max over ranks.  The KV cache rotates
-through enough copies (>= 3x the L2 size) that every call reads from HBM.
-The library records per-kernel CUDA events inside the same graphs; the
-partial kernel's mean duration in the timed region gives the roofline line.
+Timing: W eager warm-up calls, then one replay of a CUDA graph of EXACTLY
+K back-to-back calls (the same structure for every K), bracketed by a
+barrier and a synchronize on both sides, timed with CUDA events on the
+launching stream; max over ranks.  The KV cache rotates through enough
+copies (>= 3x the L2 size) that every call reads from HBM.  A twin of that
+graph, in which the library records per-kernel CUDA events, is replayed
+right after: the partial kernel's mean duration there gives the roofline
+line.  A second figure, median and p95 of 30 single-call replays after 10
+warm-ups, gives the latency of one call.
 
-``--impl reference`` times the fp64 CPU oracle (the reference arm) on a
-bounded sample of the same workload.
+``--impl reference`` and the cpu_baseline leg time the fp64 CPU oracle as it
+stands, one process per host core, on the same workload.
 
 Multi-GPU: the path does not shard inside one call; N ranks run N
 independent replicas ("weak" scaling) and ``value`` sums their KV bytes
@@ -30,8 +33,9 @@ import sys
 import tempfile
 import time
 
-# The CPU legs (oracle timing) run on one host thread; keep any BLAS
-# library numpy may load to one thread so ``cores`` stays true.
+# The CPU legs (oracle timing) run one process per host core, each on one
+# thread; keep any BLAS library numpy may load to one thread so ``cores``
+# stays true.
 for _var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_var, "1")
 
@@ -56,7 +60,6 @@ def parse():
     ap.add_argument("--steps", type=int, default=600)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-sample-kv-heads", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kernel", default="auto", choices=["auto", "cuda-cores"])
@@ -153,74 +156,117 @@ def replica_value(kv_bytes: int, steps: int, ms: float, world: int):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (reference arm and cpu_baseline).
 
-def oracle_sample(case, kv_heads: int):
-    """Run the oracle on every (row, head) of the first ``kv_heads`` KV heads
-    of the case; returns (seconds, fraction of the call's KV bytes)."""
+_ORACLE_CASE = None
+
+
+def _oracle_init(ctx):
+    global _ORACLE_CASE
+    import synthetic as sy
+    _ORACLE_CASE = sy.long_q8(ctx=ctx, num_splits=SPLITS)
+
+
+def _oracle_task(job):
+    rows, heads = job
     import oracle
-    G = case.num_heads // case.num_kv_heads
-    heads = list(range(kv_heads * G))
-    t = time.perf_counter()
-    oracle.verify_case(case, heads=heads)
-    dt = time.perf_counter() - t
-    return dt, kv_heads / case.num_kv_heads
+    oracle.verify_case(_ORACLE_CASE, rows=rows, heads=heads)
+    return len(rows) * len(heads)
 
 
-def cpu_baseline(case, kv_heads: int, min_seconds: float = 10.0):
-    """The oracle as it stands on ``kv_heads`` KV heads of the call, repeated
-    until at least ``min_seconds`` of CPU work have been timed."""
-    total, done, reps = 0.0, 0.0, 0
+class OraclePool:
+    """The fp64 oracle as it stands, spread over the host's cores: spawned
+    worker processes (started before any GPU work; spawning is safe after it
+    too), each holding the ctx-32768 call, run oracle.verify_case on
+    (query rows x the query heads of one KV head) jobs."""
+
+    def __init__(self, ctx=HEADLINE_CTX, procs=None):
+        import multiprocessing as mp
+        self.procs = procs or max(1, os.cpu_count() or 1)
+        self.pool = mp.get_context("spawn").Pool(self.procs, initializer=_oracle_init,
+                                                 initargs=(ctx,))
+        import synthetic as sy
+        self.case = sy.long_q8(ctx=ctx, num_splits=SPLITS)
+        c = self.case
+        self.G = c.num_heads // c.num_kv_heads
+        self.pairs_total = c.total_rows * c.num_heads
+        # every worker has built the case before anything is timed
+        self.pool.map(_oracle_task, [([0], [0])] * self.procs, chunksize=1)
+
+    def jobs(self, rows, kv_heads):
+        """(rows, heads) jobs covering ``rows`` x the heads of ``kv_heads``,
+        split so that every process gets work."""
+        per_kv = max(1, -(-self.procs // max(1, len(kv_heads))))
+        groups = [rows[i::per_kv] for i in range(min(per_kv, len(rows)))]
+        return [(g, list(range(k * self.G, (k + 1) * self.G))) for k in kv_heads for g in groups]
+
+    def run(self, jobs):
+        """Wall seconds and (row, head) pairs of one parallel pass."""
+        t = time.perf_counter()
+        n = sum(self.pool.map(_oracle_task, jobs, chunksize=1))
+        return time.perf_counter() - t, n
+
+    def close(self):
+        self.pool.terminate()
+
+
+def cpu_baseline(min_seconds: float = 10.0):
+    """The oracle as it stands on the host's cores: whole ctx-32768 calls
+    (every row and head), repeated until at least ``min_seconds`` of wall
+    time have been timed."""
+    op = OraclePool()
+    c = op.case
+    jobs = op.jobs(list(range(c.total_rows)), list(range(c.num_kv_heads)))
+    total, pairs, reps = 0.0, 0, 0
     while total < min_seconds:
-        dt, frac = oracle_sample(case, kv_heads)
+        dt, n = op.run(jobs)
         total += dt
-        done += frac
+        pairs += n
         reps += 1
-    gbs = case.kv_bytes * done / total / 1e9
-    return {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"fp64 numpy oracle, single thread: all 16 rows x {kv_heads * 6} query heads "
-                      f"({kv_heads} of 4 KV heads) of one ctx-{case.ctx_len[0]} call, "
-                      f"{reps} times, {total:.1f} s; GB/s = those shares of the call's KV "
-                      f"bytes / time"}
+    op.close()
+    gbs = c.kv_bytes * (pairs / op.pairs_total) / total / 1e9
+    return {"value": gbs, "unit": UNIT, "cores": op.procs, "kind": "oracle",
+            "sample": f"fp64 numpy oracle on {op.procs} processes (one thread each): every "
+                      f"query row and head of one ctx-{HEADLINE_CTX} call, {reps} calls in "
+                      f"{total:.1f} s wall; GB/s = the calls' KV bytes / wall time"}
 
 
 def run_reference(args):
-    """The oracle as it stands, timed on the host cores: each step runs it on
-    a bounded sample of the ctx-32768 call (whole query rows x heads of one
-    KV head, sized so that the whole run stays within a few minutes)."""
+    """The oracle as it stands, timed on the host's cores: each step runs it on
+    a bounded sample of the ctx-32768 call (whole query rows x the heads of
+    whole KV heads, spread over the cores, sized so that the whole run stays
+    within a few minutes)."""
     world, rank, _ = dist_setup_cpu()
     if rank != 0:
         return
-    import oracle
-    import synthetic as sy
-    case = sy.long_q8(ctx=HEADLINE_CTX, num_splits=SPLITS)
-    G = case.num_heads // case.num_kv_heads
-    pairs_total = case.total_rows * case.num_heads
-
-    def step(rows, heads):
-        t = time.perf_counter()
-        oracle.verify_case(case, rows=rows, heads=heads)
-        return time.perf_counter() - t
-
-    # Calibrate on the smallest sample, then take the largest sample whose
-    # estimated cost keeps all steps within the budget.
+    op = OraclePool()
+    c = op.case
+    all_rows = list(range(c.total_rows))
     budget_s = 150.0
-    c1 = step([0], [0])
-    all_rows = list(range(case.total_rows))
-    choices = [(all_rows, list(range(G)), 14.0), (all_rows, [0], 2.5), ([0], [0], 1.0)]
-    rows, heads = choices[-1][:2]
-    for r, h, rel in choices:
-        if rel * c1 * (args.steps + args.warmup) <= budget_s:
-            rows, heads = r, h
+    # Calibrate on one whole call, then take the largest sample whose cost
+    # keeps every step within the budget.
+    t_call, _ = op.run(op.jobs(all_rows, list(range(c.num_kv_heads))))
+    choices = [(all_rows, list(range(c.num_kv_heads)), 1.0), (all_rows, [0], 0.3),
+               (all_rows[:op.procs], [0], 0.1)]
+    rows, kvs = choices[-1][:2]
+    for r, k, rel in choices:
+        if rel * t_call * (args.steps + args.warmup) <= budget_s:
+            rows, kvs = r, k
             break
+    jobs = op.jobs(rows, kvs)
     for _ in range(args.warmup):
-        step(rows, heads)
-    times = [step(rows, heads) for _ in range(args.steps)]
+        op.run(jobs)
+    times, pairs = [], 0
+    for _ in range(args.steps):
+        dt, n = op.run(jobs)
+        times.append(dt)
+        pairs += n
+    op.close()
     total = sum(times)
-    frac = len(rows) * len(heads) / pairs_total
-    gbs = case.kv_bytes * frac * len(times) / total / 1e9
+    gbs = c.kv_bytes * (pairs / op.pairs_total) / total / 1e9
     ms = total / len(times) * 1e3
-    sample = (f"each step: the fp64 oracle on {len(rows)} of {case.total_rows} query rows x "
-              f"{len(heads)} of {case.num_heads} heads of one ctx-{HEADLINE_CTX} call; GB/s = "
-              f"that share of the call's KV bytes / time")
+    sample = (f"each step: the fp64 oracle on {op.procs} processes over {len(rows)} of "
+              f"{c.total_rows} query rows x the heads of {len(kvs)} of {c.num_kv_heads} KV heads "
+              f"of one ctx-{HEADLINE_CTX} call; GB/s = that share of the call's KV bytes / wall "
+              f"time")
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -228,7 +274,7 @@ def run_reference(args):
             "config": {"workload": f"long-context Q8 verify: 1 seq, B=16 chain, H24/KV4/D256, "
                                    f"Q8_0 KV (bf16 Q), ctx {HEADLINE_CTX}, split-KV S={SPLITS}",
                        "sample": sample},
-            "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": op.procs, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": gbs, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -328,48 +374,47 @@ class Bench:
         self.va.verify_attn(self.p, self.kvs[i % self.copies], self.mode, ws=self.ws, o=self.o,
                             lse=self.lse, status=self.status, stream=self.stream)
 
-    def capture(self, calls_per_graph):
+    def capture(self, steps):
+        """One graph of exactly ``steps`` back-to-back calls (call i reads KV
+        copy i % copies), its instrumented twin (the library records
+        per-kernel CUDA events inside it; an event between the partial and
+        merge kernels also stops the merge's early, programmatic launch, so
+        the plain graph gives the per-call time and the twin the per-kernel
+        durations), and one single-call graph per KV copy."""
         import torch
         torch.cuda.synchronize()
-        self.singles = []
-        for i in range(self.copies):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=self.stream):
-                self.call(i)
-            self.singles.append(g)
-        self.block_calls = calls_per_graph
+        self.steps = steps
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=self.stream):
-            for i in range(calls_per_graph):
+            for i in range(steps):
                 self.call(i)
-        self.block = g
-        # The instrumented copy: the library records per-kernel events inside
-        # the graph (created eagerly first).  An event between the partial
-        # and merge kernels also stops the merge's early (programmatic)
-        # launch, so the plain graph gives the per-call time and this one the
-        # per-kernel durations.
+        self.graph = g
+        # The twin's events are created by eager calls first (slots are
+        # reused from 0 each time timing is switched on).
         self.va.timing_enable(True)
-        for i in range(calls_per_graph):
+        for i in range(steps):
             self.call(i)
         torch.cuda.synchronize()
         self.va.timing_enable(True)
         g2 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g2, stream=self.stream):
-            for i in range(calls_per_graph):
+            for i in range(steps):
                 self.call(i)
         self.va.timing_enable(False)
-        self.block_timed = g2
+        self.graph_timed = g2
+        self.singles = []
+        for i in range(self.copies):
+            g1 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g1, stream=self.stream):
+                self.call(i)
+            self.singles.append(g1)
         torch.cuda.synchronize()
 
-    def replay(self, calls, instrumented=False):
-        nb, rem = divmod(calls, self.block_calls)
-        blk = self.block_timed if instrumented else self.block
-        for _ in range(nb):
-            blk.replay()
-        for i in range(rem):
-            self.singles[i % self.copies].replay()
-
-    def timed(self, calls, world, instrumented=False):
+    def timed(self, world, instrumented=False):
+        """Milliseconds of one replay of the ``steps``-call graph, between a
+        barrier + synchronize on both sides; with ``instrumented`` also each
+        call's (partial, merge) kernel milliseconds, read from the events
+        recorded in that replay."""
         import torch
         torch.cuda.synchronize()
         barrier(world)
@@ -378,11 +423,41 @@ class Bench:
         e1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(self.stream):
             e0.record(self.stream)
-            self.replay(calls, instrumented)
+            (self.graph_timed if instrumented else self.graph).replay()
             e1.record(self.stream)
         torch.cuda.synchronize()
         barrier(world)
-        return e0.elapsed_time(e1)
+        ms = e0.elapsed_time(e1)
+        if not instrumented:
+            return ms
+        return ms, self.va.timing_read(self.steps)
+
+    def single_call_us(self, warmup=10, measurements=30):
+        """Latency of one call: a single-call graph (KV copy rotating, so the
+        KV comes from HBM) timed alone, synchronised on both sides; ``warmup``
+        untimed, then ``measurements`` timed."""
+        import torch
+        out = []
+        for i in range(warmup + measurements):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(self.stream):
+                e0.record(self.stream)
+                self.singles[i % self.copies].replay()
+                e1.record(self.stream)
+            torch.cuda.synchronize()
+            if i >= warmup:
+                out.append(e0.elapsed_time(e1) * 1e3)
+        return {"median_us": float(np.median(out)), "p95_us": float(np.percentile(out, 95)),
+                "measurements": measurements, "warmup": warmup}
+
+    def run_for(self, seconds):
+        import torch
+        t_end = time.time() + seconds
+        while time.time() < t_end:
+            self.graph.replay()
+            torch.cuda.synchronize()
 
 
 def e2e_measure(case, steps, warmup, flags):
@@ -447,8 +522,7 @@ def run_ours(args):
     # CPU baseline first (rank 0, N=1 only), before any GPU work.
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(sy.long_q8(ctx=HEADLINE_CTX, num_splits=SPLITS),
-                           args.cpu_sample_kv_heads)
+        cpu = cpu_baseline()
 
     case = sy.long_q8(ctx=HEADLINE_CTX, num_splits=SPLITS, seed=1003 + rank)
     b = Bench(case, flags, l2)
@@ -456,82 +530,76 @@ def run_ours(args):
         b.call(i)
     torch.cuda.synchronize()
     assert int(b.status.item()) == 0, "device status set during warm-up"
-    calls_per_graph = 4 * b.copies
-    b.capture(calls_per_graph)
+    b.capture(args.steps)
 
     # Sustained load around the timed region so the clock sampler sees it.
     gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local)
     sampler = ClockSampler(gpu_id) if rank == 0 else None
     if sampler:
         sampler.start()
-    t_end = time.time() + 1.0
-    while time.time() < t_end:
-        b.replay(calls_per_graph * 8)
-        torch.cuda.synchronize()
-    ms = b.timed(args.steps, world)
-    ms_instr = b.timed(args.steps, world, instrumented=True)
+    b.run_for(1.0)
+    ms = b.timed(world)
+    ms_instr, (partial_ms, merge_ms) = b.timed(world, instrumented=True)
     assert int(b.status.item()) == 0, f"device status {int(b.status.item()):#x} in the timed region"
-    partial_ms, merge_ms = va.timing_read(calls_per_graph)
-    t_end = time.time() + 0.5
-    while time.time() < t_end:
-        b.replay(calls_per_graph * 8)
-        torch.cuda.synchronize()
+    b.run_for(0.5)
     clocks = sampler.stop() if sampler else None
+    latency = b.single_call_us()
     value, ms_max = replica_value(case.kv_bytes, args.steps, ms, world)
     per_call_ms = ms_max / args.steps
     part_us = float(np.mean(partial_ms)) * 1e3 if partial_ms else None
     merge_us = float(np.mean(merge_ms)) * 1e3 if merge_ms else None
     achieved = case.kv_bytes / (part_us * 1e-6) / 1e9 if part_us else None
 
+    def measure(c, n):
+        """Per-call µs of one replay of an n-call graph, the partial and merge
+        kernels' mean µs from its instrumented twin, and the single-call
+        latency figure."""
+        bb = Bench(c, flags, l2)
+        for i in range(3):
+            bb.call(i)
+        bb.capture(n)
+        ms_ = max_over_ranks(bb.timed(world), world)
+        assert int(bb.status.item()) == 0, f"{c.name}: device status {int(bb.status.item()):#x}"
+        _, (pm, mm) = bb.timed(world, instrumented=True)
+        us = ms_ / n * 1e3
+        out = {"us_per_call": us, "kv_bytes_per_call": c.kv_bytes,
+               "kv_gbs": c.kv_bytes / (us * 1e-6) / 1e9,
+               "hbm_frac": c.kv_bytes / (us * 1e-6) / 1e9 / peak,
+               "partial_us": float(np.mean(pm)) * 1e3, "merge_us": float(np.mean(mm)) * 1e3,
+               "single_call": bb.single_call_us(),
+               "kernel": KERNEL_NAMES[bb.plan["kernel"]], "chunks": bb.plan["slots"],
+               "graph_calls": n}
+        del bb
+        return out
+
+    n_other = min(args.steps, 200)
     contexts = {}
     for ctx in OTHER_CTX + [HEADLINE_CTX]:
         if ctx == HEADLINE_CTX:
             us = per_call_ms * 1e3
             contexts[str(ctx)] = {"us_per_call": us,
                                   "kv_gbs": case.kv_bytes / (us * 1e-6) / 1e9,
-                                  "partial_us": part_us, "merge_us": merge_us}
+                                  "partial_us": part_us, "merge_us": merge_us,
+                                  "single_call": latency, "chunks": b.plan["slots"],
+                                  "graph_calls": args.steps}
             continue
-        c2 = sy.long_q8(ctx=ctx, num_splits=SPLITS, seed=1003 + rank)
-        b2 = Bench(c2, flags, l2)
-        for i in range(3):
-            b2.call(i)
-        b2.capture(4 * b2.copies)
-        n2 = max(4 * b2.copies, min(args.steps, 400))
-        ms2 = max_over_ranks(b2.timed(n2, world), world)
-        assert int(b2.status.item()) == 0, f"ctx {ctx}: device status {int(b2.status.item()):#x}"
-        b2.timed(n2, world, instrumented=True)
-        pm, mm = va.timing_read(4 * b2.copies)
-        us = ms2 / n2 * 1e3
-        contexts[str(ctx)] = {"us_per_call": us, "kv_gbs": c2.kv_bytes / (us * 1e-6) / 1e9,
-                              "partial_us": float(np.mean(pm)) * 1e3,
-                              "merge_us": float(np.mean(mm)) * 1e3}
-        del b2
+        contexts[str(ctx)] = measure(sy.long_q8(ctx=ctx, num_splits=SPLITS, seed=1003 + rank),
+                                     n_other)
 
     # The other verify workloads (context for the headline; same method:
-    # rotating KV copies >= 3x L2, graphs of library calls, CUDA events).
+    # rotating KV copies >= 3x L2, one graph of n library calls, CUDA events).
     workloads = {}
     if not args.no_workloads:
-        for name, make in [("dflash-bf16 ctx4096 S8", lambda: sy.dflash_bf16(ctx=4096, num_splits=8)),
+        for name, make in [("dflash-bf16 ctx1024 S8", lambda: sy.dflash_bf16(ctx=1024, num_splits=8)),
+                           ("dflash-bf16 ctx4096 S8", lambda: sy.dflash_bf16(ctx=4096, num_splits=8)),
                            ("dflash-bf16 ctx8192 S8", lambda: sy.dflash_bf16(ctx=8192, num_splits=8)),
+                           ("long-q8 ctx1024 S8", lambda: sy.long_q8(ctx=1024, num_splits=8)),
+                           ("long-q8 ctx4096 S8", lambda: sy.long_q8(ctx=4096, num_splits=8)),
                            ("paged-d128 bf16 4x~29K S8", lambda: sy.paged_d128()),
                            ("paged-d128 Q8 4x~29K S8", lambda: sy.paged_d128(kv_dtype=sy.Q8_0)),
                            ("mixed tree+direct Q8 paged S8", lambda: sy.mixed_tree_direct()),
                            ("mixed prefill-256+direct+tree Q8 paged S8", lambda: sy.mixed_prefill())]:
-            c3 = make()
-            b3 = Bench(c3, flags, l2)
-            for i in range(3):
-                b3.call(i)
-            b3.capture(2 * b3.copies)
-            n3 = max(2 * b3.copies, min(args.steps, 200) // (2 * b3.copies) * (2 * b3.copies))
-            ms3 = max_over_ranks(b3.timed(n3, world), world)
-            assert int(b3.status.item()) == 0, f"{name}: device status {int(b3.status.item()):#x}"
-            us = ms3 / n3 * 1e3
-            workloads[name] = {"us_per_call": us, "kv_bytes_per_call": c3.kv_bytes,
-                               "kv_gbs": c3.kv_bytes / (us * 1e-6) / 1e9,
-                               "hbm_frac": c3.kv_bytes / (us * 1e-6) / 1e9 / peak,
-                               "kernel": KERNEL_NAMES[b3.plan["kernel"]],
-                               "slots": b3.plan["slots"]}
-            del b3
+            workloads[name] = measure(make(), n_other)
 
     e2e = None
     if not args.no_e2e:
@@ -548,20 +616,27 @@ def run_ours(args):
         "dtype": "f16" if b.plan["kernel"] != 0 else "f32",
         "data": "synthetic",
         "config": {"workload": f"long-context Q8 verify: 1 seq, B=16 chain, H24/KV4/D256, Q8_0 "
-                               f"KV (bf16 Q), ctx {HEADLINE_CTX}, split-KV S={SPLITS}",
+                               f"KV (bf16 Q), ctx {HEADLINE_CTX}, split-KV S={SPLITS} -> "
+                               f"{b.plan['slots']} chunks",
                    "kv_bytes_per_call": case.kv_bytes, "seed": 1003,
                    "l2": f"KV rotates through {b.copies} copies "
                          f"({b.copies * b.kv.k.numel() * 2 / 2 ** 20:.0f} MiB >= 3x L2 "
                          f"{l2 / 2 ** 20:.0f} MiB)",
-                   "launch": "CUDA graphs of library calls, "
-                             f"{calls_per_graph} calls per graph; merge launched as a "
-                             "programmatic dependent of the partial kernel",
-                   "kernel_timing": "per-kernel CUDA events recorded by the library inside "
-                                    "an identical graph, timed right after the headline "
-                                    "region over the same number of calls",
+                   "launch": f"one CUDA graph of exactly steps = {args.steps} back-to-back "
+                             "library calls, replayed once in the timed region; merge "
+                             "launched as a programmatic dependent of the partial kernel",
+                   "kernel_timing": "partial_us / merge_us: mean of the per-kernel CUDA events "
+                                    "the library records inside a twin of that graph (same "
+                                    f"{args.steps} calls), replayed once right after the "
+                                    "headline region",
+                   "single_call": "median and p95 of 30 single-call graph replays after 10 "
+                                  "warm-ups, each synchronised on both sides",
                    "plan": b.plan},
         "us_per_call": per_call_ms * 1e3,
         "us_per_call_instrumented": ms_instr / args.steps * 1e3,
+        "single_call_us": latency,
+        "partial_us": part_us,
+        "merge_us": merge_us,
         "hbm_frac_call": value / world / peak,
         "contexts": contexts,
         "workloads": workloads,
