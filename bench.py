@@ -69,17 +69,22 @@ def parse():
                     help="profiling run for ncu: W + K eager calls of the headline workload "
                          "(--ctx selects the context), no graphs, no JSON line")
     ap.add_argument("--ctx", type=int, default=HEADLINE_CTX)
+    ap.add_argument("--workload", default="long-q8",
+                    choices=["long-q8", "mixed-tree-direct", "paged-d128-q8", "dflash-bf16"],
+                    help="--profile only: the workload whose calls are run (--ctx applies to "
+                         "long-q8 and dflash-bf16)")
     return ap.parse_args()
 
 
-# DRAM bytes (read + write) of one tensor-core partial launch on the
-# ctx-32768 workload, from the full ncu capture summarised under profiles/.
-# Reported only while the kernel sources (comments and white space aside)
-# are the ones it was taken on.
+# DRAM bytes (read + write) of one Q8 tensor-core partial launch on the
+# ctx-32768 workload (71,696,896 read + 2,077,952 written), from the ncu
+# capture summarised in profiles/tq8_partial_q8_ctx32768.md.  Reported only
+# while the kernel sources (comments and white space aside) are the ones it
+# was taken on.
 PROFILED_TRAFFIC = {
-    "bytes": 73_513_984,
-    "sources": {"va_umma.cu": "03910589e6bcca2d", "va_common.cuh": "69f96982534defe0",
-                "va_sm100.cuh": "5d2883a00bf72a31"},
+    "bytes": 73_774_848,
+    "sources": {"va_tq8.cu": "f34c38911420e5e7", "va_common.cuh": "69f96982534defe0",
+                "va_sm100.cuh": "ff735fa02c94f492"},
 }
 
 
@@ -664,14 +669,17 @@ def run_profile(args):
     import synthetic as sy
     torch.cuda.set_device(0)
     flags = va.FLAG_CUDA_CORES if args.kernel == "cuda-cores" else 0
-    case = sy.long_q8(ctx=args.ctx, num_splits=SPLITS)
+    case = {"long-q8": lambda: sy.long_q8(ctx=args.ctx, num_splits=SPLITS),
+            "mixed-tree-direct": lambda: sy.mixed_tree_direct(),
+            "paged-d128-q8": lambda: sy.paged_d128(kv_dtype=sy.Q8_0),
+            "dflash-bf16": lambda: sy.dflash_bf16(ctx=args.ctx, num_splits=SPLITS)}[args.workload]()
     l2 = int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2 ** 20))
     b = Bench(case, flags, l2)
     for i in range(args.warmup + args.steps):
         b.call(i)
     torch.cuda.synchronize()
     st = int(b.status.item())
-    print(f"profile run: {args.warmup + args.steps} calls, ctx {args.ctx}, status {st:#x}, "
+    print(f"profile run: {args.warmup + args.steps} calls of {case.name}, status {st:#x}, "
           f"plan {b.plan}")
     if st:
         sys.exit(1)

@@ -134,18 +134,20 @@ struct Plan {
 static Plan make_plan(const va_problem* p, const va_kv* kv) {
   Plan pl;
   const int G = p->num_heads / kv->num_kv_heads;
-  // Kernel choice from the cache dtype, the caller's flag and whether a
-  // tree scratch KV is given, never from the problem's sizes: Q8_0 caches
-  // run on the transposed tensor-core kernel (any layout, with or without
-  // a scratch KV), bf16 caches on the row-major tensor-core kernel (no
-  // scratch KV), everything else on the CUDA-core kernel.
+  // Kernel choice from the cache dtype, the layout, the caller's flag and
+  // whether a tree scratch KV is given, never from the problem's sizes:
+  // the row-major tensor-core kernel for bf16 caches without a scratch KV
+  // and for Q8_0 caches except contiguous ones with a scratch KV, which the
+  // transposed tensor-core kernel takes; everything else on the CUDA-core
+  // kernel.
   const bool tensor_ok = kv->dtype != VA_F32 && !(p->flags & VA_FLAG_CUDA_CORES);
-  if (tensor_ok && kv->dtype == VA_Q8_0) {
+  const bool scratch = kv->draft_k != nullptr;
+  if (tensor_ok && kv->dtype == VA_Q8_0 && kv->page_size == 0 && scratch) {
     pl.kernel = VA_KERNEL_TENSOR_Q8;
     pl.rows_per_block = tq8_rows_per_block();
     pl.threads = tq8_threads();
     pl.smem = tq8_smem_bytes(kv->head_dim);
-  } else if (tensor_ok && !kv->draft_k) {
+  } else if (tensor_ok && (!scratch || kv->dtype == VA_Q8_0)) {
     pl.kernel = VA_KERNEL_TENSOR;
     pl.rows_per_block = kUmmaRowsPerBlock;
     pl.threads = umma_threads(kv->head_dim, kv->dtype);

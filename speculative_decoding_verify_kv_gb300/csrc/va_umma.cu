@@ -7,7 +7,9 @@
 // across several verifier rows; here across all of them).  Per 64-token
 // tile:
 //
-//   S = Q K^T      tcgen05.mma, A = Q (TMEM), B = K tile (smem, K-major)
+//   S = Q K^T      tcgen05.mma, A = Q (TMEM), B = K tile (smem, K-major);
+//                  Q8: one MMA for K's fp16 hi parts and one for its lo
+//                  parts per K step
 //   softmax        8 warps, one TMEM lane (= query row) per thread and one
 //                  half of the tile's columns per warp; masks (chain rows
 //                  causal by index, tree rows by ancestor mask); online
@@ -22,8 +24,11 @@
 // Caches:
 //   Q8_0, contiguous: a tile's raw 34-byte blocks arrive by one 1-D bulk
 //     copy per tensor into a tile buffer; four warps per tensor dequantise
-//     them in place to fp16 (one rounding of d*q) in the 128-byte-swizzled
-//     MMA layout, zero-filling tokens past the range.  Paged (a separate
+//     them in place to fp16 in the 128-byte-swizzled MMA layout,
+//     zero-filling tokens past the range.  A K element d*q (up to 19
+//     significant bits) becomes hi = fp16(d*q) in place and the residual
+//     lo = fma(d, q, -hi), exact in fp16, in a K-lo tile, so the two S MMAs
+//     see d*q exactly; V elements are fp16(d*q) (one rounding).  Paged (a separate
 //     instantiation): the same warps load the raw rows themselves through
 //     the block table (a tree sequence's drafts from the tree scratch KV
 //     when one is given).  Q is converted to fp16 after a per-row power-of-two
@@ -40,6 +45,7 @@
 // fixes up V tails.
 // Every wait is bounded (VA_DEV_TIMEOUT); on a timeout the CTA drains its
 // own copies and MMAs, frees TMEM and writes NaN partials.
+#include <limits.h>
 #include <string.h>
 
 #include "va_common.cuh"
@@ -60,7 +66,7 @@ struct UCfg {
   static constexpr int NB = D / 32;                      // Q8 blocks per row
   static constexpr int DBLK = D / 64;                    // 64-element column blocks
   static constexpr int TILE = kNT * D * 2;               // one 16-bit tile in smem
-  static constexpr int NB16 = 3;                         // Q8 tile buffers per tensor
+  static constexpr int NB16 = 2;                         // Q8 tile buffers per tensor
   static constexpr int NST = (D == 256) ? 3 : (D == 128 ? 6 : 8);  // bf16 K+V stages
   static constexpr int COL_O = 0;
   static constexpr int COL_S0 = D;
@@ -73,7 +79,7 @@ struct UCfg {
   static constexpr int PV_WARP = kQ8 ? 13 : 11;
   static constexpr int THREADS = (kQ8 ? 20 : 12) * 32;
   static constexpr int MAXREG = (65536 / THREADS) / 8 * 8 > 255 ? 255 : (65536 / THREADS) / 8 * 8;
-  static constexpr int SMEM_Q8 = 2 * NB16 * TILE;
+  static constexpr int SMEM_Q8 = 3 * NB16 * TILE;       // K, V and K-lo tiles
   static constexpr int SMEM_BF16 = NST * 2 * TILE;
   static constexpr int SMEM_EPI = kM * (D * 4 + 16);  // O staging at the end
   static constexpr int SMEM_MAIN = kQ8 ? SMEM_Q8 : SMEM_BF16;
@@ -129,6 +135,59 @@ __device__ __forceinline__ void named_barrier_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// One Q8_0 block (fp16 scale d, 32 int8 codes q) held in words w from
+// word wo (odd: the block starts two bytes into w[wo]; live false: zeros)
+// -> fp16 hi = fp16(d*q) into the 16-byte chunks c0 .. c0 + 3 of token row
+// t of the swizzled column block hi.  With lo (K tiles), also the residuals
+// fma(d, q, -hi) into the same place of lo: a residual of d*q (at most 19
+// significant bits) below hi's last bit fits fp16 exactly, so hi + lo ==
+// d*q and the S MMAs over both parts see the exact K element.  A chunk is
+// stored as soon as it is converted, to keep few values in registers.
+__device__ __forceinline__ void dq_block_store(const uint32_t* w, int wo, bool odd, bool live,
+                                               unsigned char* hi, unsigned char* lo, int t, int c0) {
+  uint32_t sbits = 0u, code[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) code[q] = 0u;
+  if (live) {
+    if (odd) {
+      sbits = w[wo] >> 16;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) code[q] = w[wo + 1 + q];
+    } else {
+      sbits = w[wo] & 0xFFFFu;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) code[q] = __funnelshift_r(w[wo + q], w[wo + q + 1], 16);
+    }
+  }
+  const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)sbits));
+  const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t hv[4], lv[4];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t x = code[2 * c + k] ^ 0x80808080u;  // bytes q + 128
+      uint32_t b0 = __byte_perm(x, 0x64646464u, 0x4140);
+      uint32_t b1 = __byte_perm(x, 0x64646464u, 0x4342);
+      const __half2 q0 = __hsub2(*reinterpret_cast<__half2*>(&b0), bias);  // exact codes
+      const __half2 q1 = __hsub2(*reinterpret_cast<__half2*>(&b1), bias);
+      __half2 a = __hmul2(q0, d2);
+      __half2 e = __hmul2(q1, d2);
+      hv[2 * k] = *reinterpret_cast<uint32_t*>(&a);
+      hv[2 * k + 1] = *reinterpret_cast<uint32_t*>(&e);
+      if (lo) {
+        __half2 la = __hfma2(q0, d2, __hneg2(a));
+        __half2 le = __hfma2(q1, d2, __hneg2(e));
+        lv[2 * k] = *reinterpret_cast<uint32_t*>(&la);
+        lv[2 * k + 1] = *reinterpret_cast<uint32_t*>(&le);
+      }
+    }
+    const uint32_t off = sw128_off(t, c0 + c);
+    *reinterpret_cast<uint4*>(hi + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    if (lo) *reinterpret_cast<uint4*>(lo + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+  }
+}
+
 // Q8_0 dequantisation by direct loads (paged caches).  A thread owns one
 // half-row (token t = gtid % 64 of the tile, half hf = gtid / 64 of its
 // D/32 blocks).  It loads the raw bytes of its half-row from global memory
@@ -175,66 +234,30 @@ __device__ __forceinline__ void dq_load(DqRaw<D>& r, const unsigned char* row, i
 // Convert and store; SH = byte offset of the half-row's first block within
 // the loaded words.
 template <int D, int SH>
-__device__ __forceinline__ void dq_store(const DqRaw<D>& r, unsigned char* buf, int t, int hf,
-                                         bool live) {
+__device__ __forceinline__ void dq_store(const DqRaw<D>& r, unsigned char* buf, unsigned char* lobuf,
+                                         int t, int hf, bool live) {
   constexpr int NBH = D / 64;                     // blocks per half-row
 #pragma unroll
   for (int jb = 0; jb < NBH; ++jb) {
     const int b = hf * NBH + jb;                  // block index in the row
-    unsigned char* drow = buf + (b >> 1) * (kNT * 128);
-    const int c0 = (b & 1) * 4;
-    uint4 out[4];
-    if (live) {
-      constexpr int O0 = SH;
-      const int o = O0 + 34 * jb;                 // block offset in the loaded bytes
-      const int wo = o >> 2;
-      uint32_t sbits, code[8];
-      if (o & 2) {
-        sbits = r.w[wo] >> 16;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) code[q] = r.w[wo + 1 + q];
-      } else {
-        sbits = r.w[wo] & 0xFFFFu;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) code[q] = __funnelshift_r(r.w[wo + q], r.w[wo + q + 1], 16);
-      }
-      const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)sbits));
-      const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
-      uint32_t hv[16];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint32_t x = code[q] ^ 0x80808080u;  // bytes q + 128
-        uint32_t lo = __byte_perm(x, 0x64646464u, 0x4140);
-        uint32_t hi = __byte_perm(x, 0x64646464u, 0x4342);
-        __half2 a = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&lo), bias), d2);
-        __half2 c = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&hi), bias), d2);
-        hv[2 * q] = *reinterpret_cast<uint32_t*>(&a);
-        hv[2 * q + 1] = *reinterpret_cast<uint32_t*>(&c);
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        out[c] = make_uint4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
-    } else {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) out[c] = make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      *reinterpret_cast<uint4*>(drow + sw128_off(t, c0 + c)) = out[c];
+    const int boff = (b >> 1) * (kNT * 128);
+    const int o = SH + 34 * jb;                   // block offset in the loaded bytes
+    dq_block_store(r.w, o >> 2, o & 2, live, buf + boff, lobuf ? lobuf + boff : nullptr, t,
+                   (b & 1) * 4);
   }
 }
 
 template <int D>
-__device__ __forceinline__ void dq_convert(const DqRaw<D>& r, unsigned char* buf, int t, int hf,
-                                           bool live) {
+__device__ __forceinline__ void dq_convert(const DqRaw<D>& r, unsigned char* buf,
+                                           unsigned char* lobuf, int t, int hf, bool live) {
   if (D == 256) {
-    if (hf) dq_store<D, 8>(r, buf, t, hf, live);
-    else dq_store<D, 0>(r, buf, t, hf, live);
+    if (hf) dq_store<D, 8>(r, buf, lobuf, t, hf, live);
+    else dq_store<D, 0>(r, buf, lobuf, t, hf, live);
   } else {
     // 4-byte loads: the half-row starts 0 or 2 bytes into the first word.
     const int sh = (hf * DqRaw<D>::HB) & 3;
-    if (sh) dq_store<D, 2>(r, buf, t, hf, live);
-    else dq_store<D, 0>(r, buf, t, hf, live);
+    if (sh) dq_store<D, 2>(r, buf, lobuf, t, hf, live);
+    else dq_store<D, 0>(r, buf, lobuf, t, hf, live);
   }
 }
 
@@ -246,8 +269,8 @@ __device__ __forceinline__ void dq_convert(const DqRaw<D>& r, unsigned char* buf
 // writes the fp16 rows (eight consecutive threads take eight consecutive
 // tokens of one block, so their 16-byte stores hit distinct bank groups).
 template <int D>
-__device__ __forceinline__ void dequant_inplace(unsigned char* buf, int valid, int tid, int barid,
-                                                bool work) {
+__device__ __forceinline__ void dequant_inplace(unsigned char* buf, unsigned char* lobuf, int valid,
+                                                int tid, int barid, bool work) {
   constexpr int NB = D / 32;      // blocks per row
   constexpr int RB = NB * 34;     // bytes per row
   constexpr int HB = RB / 2;      // bytes per half-row
@@ -289,47 +312,11 @@ __device__ __forceinline__ void dequant_inplace(unsigned char* buf, int valid, i
 #pragma unroll
   for (int jb = 0; jb < NBH; ++jb) {
     const int b = hf * NBH + jb;                 // block index in the row
-    unsigned char* drow = buf + (b >> 1) * (kNT * 128);
-    const int c0 = (b & 1) * 4;
-    uint4 out[4];
-    if (live) {
-      const int o = sh + 34 * jb;                // block offset in the thread's words
-      const int wo = o >> 2;
-      uint32_t sbits, code[8];
-      if (o & 2) {
-        sbits = w[wo] >> 16;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) code[q] = w[wo + 1 + q];
-      } else {
-        sbits = w[wo] & 0xFFFFu;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) code[q] = __funnelshift_r(w[wo + q], w[wo + q + 1], 16);
-      }
-      const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)sbits));
-      const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
-      uint32_t hv[16];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint32_t x = code[q] ^ 0x80808080u;  // bytes q + 128
-        uint32_t lo = __byte_perm(x, 0x64646464u, 0x4140);
-        uint32_t hi = __byte_perm(x, 0x64646464u, 0x4342);
-        __half2 a = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&lo), bias), d2);
-        __half2 c = __hmul2(__hsub2(*reinterpret_cast<__half2*>(&hi), bias), d2);
-        hv[2 * q] = *reinterpret_cast<uint32_t*>(&a);
-        hv[2 * q + 1] = *reinterpret_cast<uint32_t*>(&c);
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        out[c] = make_uint4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
-    } else {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) out[c] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    if (work) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(drow + sw128_off(t, c0 + c)) = out[c];
-    }
+    const int boff = (b >> 1) * (kNT * 128);
+    const int o = sh + 34 * jb;                  // block offset in the thread's words
+    if (work)
+      dq_block_store(w, o >> 2, o & 2, live, buf + boff, lobuf ? lobuf + boff : nullptr, t,
+                     (b & 1) * 4);
   }
 }
 
@@ -419,10 +406,12 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   // Shared-memory regions.
-  //   Q8: tile buffers K0 V0 K1 V1 K2 V2 (raw Q8 rows land at the start of a
-  //       buffer and are dequantised in place).
+  //   Q8: tile buffers K0 V0 K1 V1 (raw Q8 rows land at the start of a
+  //       buffer and are dequantised in place: fp16 hi parts of K, V), then
+  //       K-lo tiles L0 L1 (the residual parts of K0, K1).
   //   bf16: stages of (K tile, V tile).
   auto q8buf = [&](int kv, int j) { return sm + (2 * j + kv) * C::TILE; };
+  auto q8lo = [&](int j) { return sm + (2 * C::NB16 + j) * C::TILE; };
   auto kst = [&](int st) { return sm + st * 2 * C::TILE; };            // bf16 K stage
   auto vst = [&](int st) { return sm + st * 2 * C::TILE + C::TILE; };  // bf16 V stage
   // L2 prefetch of the raw Q8 rows of tensor kv (0 = K, 1 = V), tile i.
@@ -479,9 +468,12 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
   };
   const bool early = Q8 && p.page_size == 0 && !err && ntiles > 0;
   constexpr int kQRow = D * 2 + 16;
-  const int qslot = (min(kM, R - rb * kM) * kQRow <= 2 * C::TILE) ? 4 : 2;
+  // Q staging: the K-lo tiles L0 L1 when the block's rows fit there, else
+  // V1 L0 L1.  K-lo writes always wait until Q is in TMEM; the raw copies
+  // only in the second case, from tile 1 (buffer V1) on.
+  const int qslot = (min(kM, R - rb * kM) * kQRow <= 2 * C::TILE) ? 2 * C::NB16 : 2 * C::NB16 - 1;
   unsigned char* const qstage = sm + qslot * C::TILE;
-  const int qfirst = qslot / 2;  // first tile whose buffers hold the staging
+  const int qfirst = qslot == 2 * C::NB16 ? INT_MAX : 1;  // first tile whose raw buffers hold it
 
   if (tid == 0) {
     err_s = 0;
@@ -516,10 +508,9 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
   // Q8: warps 2.. stage this CTA's Q rows in shared memory (rows padded to
   // kQRow bytes so that the lanes of a warp read distinct bank groups) with
   // every load in flight, overlapping the rest of the prologue; the softmax
-  // warps convert them into TMEM.  The staging takes tile buffers K2 V2
-  // when the block's rows fit there (tile 1 then goes out as soon as tile 0
-  // has landed), else K1 onwards; tiles from qfirst on wait until Q is in
-  // TMEM.
+  // warps convert them into TMEM.  The staging takes the K-lo tiles when the
+  // block's rows fit there (every raw copy then goes out as soon as its
+  // buffer is free), else V1 onwards; see qslot.
   if (Q8 && warp >= 2) {
     constexpr int CPR = D / 8;  // 16-byte chunks per row
     constexpr int NTHR = C::THREADS - 64;
@@ -694,11 +685,12 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       bool any = false;
       for (int i = 0; i < ntiles && ok; ++i) {
         const int b = i & 1;
-        uint32_t kaddr;
+        uint32_t kaddr, kloaddr = 0;
         if (Q8) {
           const int jb = i % C::NB16;
           ok = mbar_wait(bar(B_QREADY8 + jb), (i / C::NB16) & 1, abort_p, kWaitNs);
           kaddr = smem_u32(q8buf(0, jb));
+          kloaddr = smem_u32(q8lo(jb));
         } else {
           const int st = i % C::NST;
           ok = mbar_wait(bar(B_RFULL + st), (i / C::NST) & 1, abort_p, kWaitNs);
@@ -709,10 +701,14 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
         if (!ok) break;
         tc_fence_after();
         const uint64_t kd0 = sdesc_sw128(kaddr, 16, 1024);
+        const uint64_t kl0 = sdesc_sw128(kloaddr, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * (kNT * 128) + (kk & 3) * 32) >> 4);
-          mma_ts(tm + C::COL_S0 + b * kNT, tm + C::COL_Q + kk * 8, kd, ID_QK, kk > 0 ? 1u : 0u);
+          const uint64_t step = (uint64_t)(((kk >> 2) * (kNT * 128) + (kk & 3) * 32) >> 4);
+          mma_ts(tm + C::COL_S0 + b * kNT, tm + C::COL_Q + kk * 8, kd0 + step, ID_QK,
+                 kk > 0 ? 1u : 0u);
+          // Q8: the K elements' residual parts (hi + lo = d*q exactly).
+          if (Q8) mma_ts(tm + C::COL_S0 + b * kNT, tm + C::COL_Q + kk * 8, kl0 + step, ID_QK, 1u);
         }
         any = true;
         mma_commit(bar(B_SFULL + b));
@@ -1023,15 +1019,18 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
           const int lo_i = i == 0 ? 1 : i + kPrefetch, hi_i = min(i + kPrefetch + 1, ntiles);
           for (int k = lo_i; k < hi_i; ++k) prefetch_q8(k, grp);
         }
+        // K writes its lo tiles, which the Q staging shares, so K always
+        // waits for Q to be in TMEM (once; later waits return at once).
         if (ok && !__all_sync(0xffffffffu,
                               mbar_wait(bar(B_QEMPTY + 3 * grp + jb), ((i / C::NB16) & 1) ^ 1,
                                         abort_p, kWaitNs) &&
-                                  (i < qfirst || mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs)))) {
+                                  ((grp == 1 && i < qfirst) ||
+                                   mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs)))) {
           ok = false;
           if (lane == 0) fail();
         }
         if (!ok) continue;
-        dq_convert<D>(raw, q8buf(grp, jb), t, hf, live);
+        dq_convert<D>(raw, q8buf(grp, jb), grp == 0 ? q8lo(jb) : nullptr, t, hf, live);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_QREADY8 + 3 * grp + jb));
@@ -1049,12 +1048,16 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       bool ok = true;
       for (int i = 0; i < ntiles; ++i) {
         const int jb = i % C::NB16;
+        // K also waits for Q to be in TMEM: its lo tiles share the staging.
         if (ok && !__all_sync(0xffffffffu, mbar_wait(bar(B_QFULL + 3 * grp + jb),
-                                                     (i / C::NB16) & 1, abort_p, kWaitNs))) {
+                                                     (i / C::NB16) & 1, abort_p, kWaitNs) &&
+                                               (grp == 1 ||
+                                                mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs)))) {
           ok = false;
           if (lane == 0) fail();
         }
-        dequant_inplace<D>(q8buf(grp, jb), shi - (slo + i * kNT), gtid, 3 + grp, ok);
+        dequant_inplace<D>(q8buf(grp, jb), grp == 0 ? q8lo(jb) : nullptr, shi - (slo + i * kNT),
+                           gtid, 3 + grp, ok);
         if (ok) {
           fence_proxy_async_smem();
           __syncwarp();

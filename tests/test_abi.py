@@ -190,13 +190,14 @@ def _sms():
 
 
 def test_plan_rule():
-    """Kernel choice and grid of va_plan (host logic only).  Kernel: Q8_0
-    caches -> the transposed tensor-core kernel (with or without a tree
-    scratch KV), bf16 caches -> the row-major tensor-core kernel (the CUDA-
-    core kernel with a scratch KV), fp32 caches or the flag -> CUDA cores.
-    Chunk count T = clamp(floor(k * SMs / KVH), S, 16 S) with k = 1 (tensor
-    cores) or 2 (CUDA cores); row blocks of 96 (Q8_0), 128 (bf16) or 16
-    (CUDA cores) query rows; one grid z per sequence."""
+    """Kernel choice and grid of va_plan (host logic only).  Kernel: the
+    row-major tensor-core kernel for bf16 caches without a tree scratch KV
+    and for Q8_0 caches except contiguous ones with a scratch KV, which take
+    the transposed tensor-core kernel; bf16 with a scratch KV, fp32 caches
+    or the flag -> CUDA cores.  Chunk count T = clamp(floor(k * SMs / KVH),
+    S, 16 S) with k = 1 (tensor cores) or 2 (CUDA cores); row blocks of 128
+    (row-major), 96 (transposed) or 16 (CUDA cores) query rows; one grid z
+    per sequence."""
     import numpy as np
     import synthetic as sy
     sms = _sms()
@@ -213,7 +214,7 @@ def test_plan_rule():
     q8 = sy.long_q8(ctx=256)                              # H24/KV4/D256, 16 rows, S = 8
     pl = plan(q8)
     T = clamp(sms // 4, 8, 128)
-    assert (pl["kernel"], pl["threads"], pl["slots"]) == (va.KERNEL_TENSOR_Q8, 512, T)
+    assert (pl["kernel"], pl["threads"], pl["slots"]) == (va.KERNEL_TENSOR, 640, T)
     assert (pl["grid_x"], pl["grid_y"], pl["grid_z"]) == (T, 4, 1)   # 96 rows: one block
     assert plan(q8, num_splits=1)["slots"] == clamp(sms // 4, 1, 16)
     simt = plan(q8, flags=va.FLAG_CUDA_CORES)
@@ -227,14 +228,16 @@ def test_plan_rule():
     long_chain = sy.make_case("c", num_heads=24, num_kv_heads=4, head_dim=256, kv_dtype=sy.Q8_0,
                               q_dtype=sy.BF16, ctx=[40], rows=[100], seed=2)
     pl = plan(long_chain, num_splits=8)
-    assert pl["grid_x"] == pl["slots"] * 7                 # 600 query rows: 7 blocks of 96
+    assert pl["grid_x"] == pl["slots"] * 5                 # 600 query rows: 5 blocks of 128
     bf_chain = sy.make_case("c", num_heads=24, num_kv_heads=4, head_dim=256, kv_dtype=sy.BF16,
                             q_dtype=sy.BF16, ctx=[40], rows=[100], seed=2)
     assert plan(bf_chain, num_splits=8)["grid_x"] == pl["slots"] * 5   # blocks of 128
     f32 = sy.tiny_chain()
     assert plan(f32)["kernel"] == va.KERNEL_CUDA_CORES
     mixed = sy.mixed_tree_direct(ctx=[40, 300, 17, 130], direct=(0, 2), num_splits=2, seed=7)
-    assert plan(mixed, scratch=True)["kernel"] == va.KERNEL_TENSOR_Q8
-    assert plan(sy.to_contiguous(mixed), scratch=True)["kernel"] == va.KERNEL_TENSOR_Q8
+    assert plan(mixed, scratch=True)["kernel"] == va.KERNEL_TENSOR
+    tq = plan(sy.to_contiguous(mixed), scratch=True)
+    assert (tq["kernel"], tq["threads"]) == (va.KERNEL_TENSOR_Q8, 512)
+    assert tq["grid_x"] == tq["slots"]          # 8 rows x G 6 = 48: one 96-row block
     assert plan(d128, num_splits=8, scratch=True)["kernel"] == va.KERNEL_CUDA_CORES
     assert np.isfinite(T)

@@ -37,10 +37,22 @@ def test_scratch_equals_drafts_in_cache_bitwise(flags):
 def test_scratch_q8_paged_runs_on_tensor_cores_and_matches_oracle():
     c = sy.with_tree_scratch(_mixed_q8_paged(402))
     p, kv, mode = va.upload(c, "cuda", num_splits=3)
-    assert va.plan(p, kv, mode)["kernel"] == va.KERNEL_TENSOR_Q8
+    assert va.plan(p, kv, mode)["kernel"] == va.KERNEL_TENSOR
     o, lse = run_gpu(c, num_splits=3)
     O, L = oracle.verify_case(c)
     compare(o, lse, O, L, "scratch q8 paged")
+
+
+def test_scratch_q8_contiguous_runs_on_the_transposed_kernel_and_matches_oracle():
+    """A contiguous Q8_0 cache with a tree scratch KV runs on the transposed
+    tensor-core kernel (tokens on M); every output against the oracle."""
+    base = sy.to_contiguous(_mixed_q8_paged(403))
+    c = sy.with_tree_scratch(base)
+    p, kv, mode = va.upload(c, "cuda", num_splits=3)
+    assert va.plan(p, kv, mode)["kernel"] == va.KERNEL_TENSOR_Q8
+    o, lse = run_gpu(c, num_splits=3)
+    O, L = oracle.verify_case(c)
+    compare(o, lse, O, L, "scratch q8 contiguous")
 
 
 @pytest.mark.parametrize("paged", [False, True])

@@ -29,7 +29,7 @@ def _sm_count():
 @pytest.mark.gpu
 @pytest.mark.parametrize("S", [1, 8])
 @pytest.mark.parametrize("dtype,flags,ctas,kernel", [
-    (sy.Q8_0, 0, 1, va.KERNEL_TENSOR_Q8),
+    (sy.Q8_0, 0, 1, va.KERNEL_TENSOR),
     (sy.BF16, 0, 1, va.KERNEL_TENSOR),
     (sy.Q8_0, va.FLAG_CUDA_CORES, 2, va.KERNEL_CUDA_CORES),
 ])
