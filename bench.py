@@ -76,14 +76,15 @@ def parse():
     return ap.parse_args()
 
 
-# DRAM bytes (read + write) of one Q8 tensor-core partial launch on the
-# ctx-32768 workload (71,696,896 read + 2,077,952 written), from the ncu
-# capture summarised in profiles/tq8_partial_q8_ctx32768.md.  Reported only
-# while the kernel sources (comments and white space aside) are the ones it
-# was taken on.
+# DRAM bytes (read + write) of one partial launch of the headline call
+# (row-major tensor-core kernel, Q8_0 with hi + lo K, ctx 32768: 71,658,240
+# read + 2,007,808 written), from the ncu capture summarised in
+# profiles/umma_partial_q8_ctx32768.md.  Reported only while the kernel
+# sources (comments and white space aside) are the ones it was taken on.
 PROFILED_TRAFFIC = {
-    "bytes": 73_774_848,
-    "sources": {"va_tq8.cu": "f34c38911420e5e7", "va_common.cuh": "69f96982534defe0",
+    "kernel": 1,
+    "bytes": 73_666_048,
+    "sources": {"va_umma.cu": "73b6698296ede266", "va_common.cuh": "69f96982534defe0",
                 "va_sm100.cuh": "ff735fa02c94f492"},
 }
 
@@ -647,7 +648,8 @@ def run_ours(args):
         "workloads": workloads,
         "roofline": {"kernel": kernel_name, "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak if achieved else None,
-                     "traffic": profiled_traffic() if b.plan["kernel"] == 2 else None,
+                     "traffic": (profiled_traffic()
+                                 if b.plan["kernel"] == PROFILED_TRAFFIC["kernel"] else None),
                      "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one "
                                        "capture of this kernel (null once it has changed)",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
