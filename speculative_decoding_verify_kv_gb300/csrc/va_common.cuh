@@ -70,15 +70,27 @@ __device__ __forceinline__ void split_range(int L, int S, int s, int* lo, int* h
 // 64-token tiles, each at least min_sub tokens: the chunk length is
 // ceil((hi - lo) / P) (or min_sub if larger) rounded up to 64; chunks past
 // the end are empty.
-__device__ __forceinline__ void sub_range(int lo, int hi, int P, int min_sub, int p, int* slo,
-                                          int* shi) {
-  const int len = hi - lo;
+__device__ __forceinline__ int sub_len(int len, int P, int min_sub) {
   int per = (len + P - 1) / P;
   if (per < min_sub) per = min_sub;
-  const int sub = (per + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
+  return (per + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
+}
+
+__device__ __forceinline__ void sub_range(int lo, int hi, int P, int min_sub, int p, int* slo,
+                                          int* shi) {
+  const int sub = sub_len(hi - lo, P, min_sub);
   long long a = lo + (long long)p * sub, b = lo + (long long)(p + 1) * sub;
   *slo = (int)(a < hi ? a : hi);
   *shi = (int)(b < hi ? b : hi);
+}
+
+// Number of non-empty chunks of [lo, hi) under sub_range (they come first).
+__device__ __forceinline__ int live_subs(int lo, int hi, int P, int min_sub) {
+  const int len = hi - lo;
+  if (len <= 0) return 0;
+  const int sub = sub_len(len, P, min_sub);
+  const int n = (len + sub - 1) / sub;
+  return n < P ? n : P;
 }
 
 // Kind of sequence s: 0 chain / direct, 1 tree.

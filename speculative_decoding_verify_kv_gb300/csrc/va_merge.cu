@@ -61,7 +61,17 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const Params p)
   int sr0, sn, sctx;
   int nan = !(p.cu_rows[s_lo] <= grow && grow < p.cu_rows[s_lo + 1]) ||
             (check_sequence(p, s_lo, &sr0, &sn, &sctx) & VA_DEV_BAD_ROWS) != 0u;
-  for (int s0 = grp; s0 < p.slots && !nan; s0 += BATCH * NG) {
+  // Slots past the sequence's last non-empty chunk hold nothing of this
+  // call: with one level of chunks they are the trailing empty ones of the
+  // partial kernels' sub_range cut, so only the first `live` are read (at
+  // least one: a sequence with rows has a non-empty span).
+  int live = p.slots;
+  if (!nan && p.S == 1 && sctx >= 0) {
+    int lo0, hi0;
+    split_range(sctx + sn, 1, 0, &lo0, &hi0);
+    live = max(1, live_subs(lo0, hi0, p.P, p.min_sub));
+  }
+  for (int s0 = grp; s0 < live && !nan; s0 += BATCH * NG) {
     float mm[BATCH], ll[BATCH];
     float4 aa[BATCH];
 #pragma unroll
@@ -70,7 +80,7 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const Params p)
       mm[k] = -INFINITY;
       ll[k] = 0.f;
       aa[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (sl < p.slots) {
+      if (sl < live) {
         const long long si = slot_index(p, sl, grow, h);
         mm[k] = p.ws_ml[2 * si];
         ll[k] = p.ws_ml[2 * si + 1];

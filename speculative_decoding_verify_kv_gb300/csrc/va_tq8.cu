@@ -265,6 +265,17 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
   split_range(L, p.S, 0, &lo, &hi);
   sub_range(lo, hi, p.P, p.min_sub, slot, &slo, &shi);
   const int ntiles = (shi - slo + kTT - 1) / kTT;
+  if (ntiles == 0 && !err) {
+    // An empty chunk (short span): its rows' slots become (-inf, 0) at once,
+    // without the prologue.  The sequence's other CTAs check its parents.
+    if (tid < Rb) {
+      const int rs = rb * kNR + tid;
+      const long long si0 = slot_index(p, slot, row0 + rs / G, kvh * G + rs % G);
+      p.ws_ml[2 * si0] = -INFINITY;
+      p.ws_ml[2 * si0 + 1] = 0.f;
+    }
+    return;
+  }
   const int kind = seq_kind_of(p, s);
   // Tree sequence with a tree scratch KV: its draft positions (>= ctx) are
   // read from the scratch rows by the dequantising threads, and the cache

@@ -385,6 +385,19 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
   split_range(L, p.S, split, &lo, &hi);
   sub_range(lo, hi, p.P, p.min_sub, sub, &slo, &shi);
   const int ntiles = (shi - slo + kNT - 1) / kNT;
+  if (ntiles == 0 && !err) {
+    // An empty chunk (short span): its rows' slots become (-inf, 0) at once,
+    // without the prologue.  The sequence's other CTAs check its parents.
+    if (tid < kM) {
+      const int rs = rb * kM + tid;
+      if (rs < R) {
+        const long long si0 = slot_index(p, slot, row0 + rs / G, kvh * G + rs % G);
+        p.ws_ml[2 * si0] = -INFINITY;
+        p.ws_ml[2 * si0 + 1] = 0.f;
+      }
+    }
+    return;
+  }
 
   // Softmax-thread row identity.
   const int quad = warp & 3;
