@@ -10,7 +10,7 @@
 //                    A = the K tile in TMEM, B = Q^T in shared memory.
 //   softmax          one thread per token: scores in log2 units against a
 //                    per-row running maximum that moves only when a score
-//                    passes it by more than 2^8 (then O^T and the row sums
+//                    passes it by more than 2^kSlack (then O^T and the row sums
 //                    are rescaled); masks (context visible to every row,
 //                    chain rows causal by index, tree rows by ancestor
 //                    mask); P = 2^(s c - m) into shared memory as fp16 P^T;
@@ -36,12 +36,13 @@
 // rounding) and P is fp16, as the P.V product's precision allows.
 //
 // Warp roles (16 warps, four warpgroups with their own register budgets):
-//   0 and 3 copy producers of K and V (raw Q8 rows into shared memory by
-//     1-D bulk copies, L2 prefetch ahead), 1 TMEM owner + S^T issuer, 2 P.V
-//     issuer;
+//   3 V producer (raw V rows into shared memory by 1-D bulk copies; L2
+//     prefetch of K and V tiles ahead), 1 TMEM owner + S^T issuer, 2 P.V
+//     issuer, 0 idle after the prologue;
 //   4..7 softmax (warp & 3 = TMEM lane quadrant = 32 tokens, every row),
 //     also the O^T rescale and the epilogue;
-//   8..11 K dequantisation (one token row per thread, into TMEM);
+//   8..11 K dequantisation (one token row per thread, read from L2, into
+//     TMEM);
 //   12..15 V dequantisation (one token row per thread, into shared memory);
 //   4..15 stage Q^T in the prologue.
 // Every wait is bounded (VA_DEV_TIMEOUT); after a timeout the CTA drains

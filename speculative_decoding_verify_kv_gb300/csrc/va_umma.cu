@@ -25,7 +25,7 @@
 //   Q8_0, contiguous: a tile's raw 34-byte blocks arrive by one 1-D bulk
 //     copy per tensor into a tile buffer; four warps per tensor dequantise
 //     them in place to fp16 in the 128-byte-swizzled MMA layout,
-//     zero-filling tokens past the range.  A K element d*q (up to 19
+//     zero-filling tokens past the range.  A K element d*q (up to 18
 //     significant bits) becomes hi = fp16(d*q) in place and the residual
 //     lo = fma(d, q, -hi), exact in fp16, in a K-lo tile, so the two S MMAs
 //     see d*q exactly; V elements are fp16(d*q) (one rounding).  Paged (a separate
@@ -94,8 +94,8 @@ enum {
   B_QREADY = 6,
   B_DRAIN = 7,    // [2] S issuer, P.V issuer
   B_OFINAL = 9,   // the last P.V has completed
-  // Q8 tile buffers, [tensor 0 = K / 1 = V][3]: raw bytes landed, fp16 ready,
-  // buffer free again.
+  // Q8 tile buffers, [tensor 0 = K / 1 = V][3 slots, NB16 used]: raw bytes
+  // landed, fp16 ready (K: hi and lo parts), buffer free again.
   B_QFULL = 10,   // [2][3]
   B_QREADY8 = 16, // [2][3]
   B_QEMPTY = 22,  // [2][3]
@@ -139,7 +139,7 @@ __device__ __forceinline__ void named_barrier_sync(int id, int count) {
 // word wo (odd: the block starts two bytes into w[wo]; live false: zeros)
 // -> fp16 hi = fp16(d*q) into the 16-byte chunks c0 .. c0 + 3 of token row
 // t of the swizzled column block hi.  With lo (K tiles), also the residuals
-// fma(d, q, -hi) into the same place of lo: a residual of d*q (at most 19
+// fma(d, q, -hi) into the same place of lo: a residual of d*q (at most 18
 // significant bits) below hi's last bit fits fp16 exactly, so hi + lo ==
 // d*q and the S MMAs over both parts see the exact K element.  A chunk is
 // stored as soon as it is converted, to keep few values in registers.
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       }
     }
   };
-  // Copy the raw Q8 rows of tensor kv, tile i, into buffer i % 3 (whose
+  // Copy the raw Q8 rows of tensor kv, tile i, into buffer i % NB16 (whose
   // previous tile must be consumed), and pull tile i + kPrefetch into L2.
   auto issue_q8 = [&](int i, int kv) {
     const int jb = i % C::NB16;
