@@ -67,6 +67,7 @@ struct UCfg {
   static constexpr int DBLK = D / 64;                    // 64-element column blocks
   static constexpr int TILE = kNT * D * 2;               // one 16-bit tile in smem
   static constexpr int NB16 = 2;                         // Q8 tile buffers per tensor
+  static constexpr int PTILE = kM * kNT * 2;             // Q8: one fp16 P tile (rows x tokens)
   static constexpr int NST = (D == 256) ? 3 : (D == 128 ? 6 : 8);  // bf16 K+V stages
   static constexpr int COL_O = 0;
   static constexpr int COL_S0 = D;
@@ -79,7 +80,9 @@ struct UCfg {
   static constexpr int PV_WARP = kQ8 ? 13 : 11;
   static constexpr int THREADS = (kQ8 ? 20 : 12) * 32;
   static constexpr int MAXREG = (65536 / THREADS) / 8 * 8 > 255 ? 255 : (65536 / THREADS) / 8 * 8;
-  static constexpr int SMEM_Q8 = 3 * NB16 * TILE;       // K, V and K-lo tiles
+  // Q8: per buffer a K tile of hi and lo parts (2 TILE) and a V tile, then
+  // the P tile.
+  static constexpr int SMEM_Q8 = 3 * NB16 * TILE + PTILE;
   static constexpr int SMEM_BF16 = NST * 2 * TILE;
   static constexpr int SMEM_EPI = kM * (D * 4 + 16);  // O staging at the end
   static constexpr int SMEM_MAIN = kQ8 ? SMEM_Q8 : SMEM_BF16;
@@ -99,6 +102,11 @@ enum {
   B_QFULL = 10,   // [2][3]
   B_QREADY8 = 16, // [2][3]
   B_QEMPTY = 22,  // [2][3]
+  // Q8 only (these slots are the bf16 stage barriers' in the other
+  // instantiation): the P.V that read the P tile completed; the softmax has
+  // read the S buffer.
+  B_PFREE = 28,
+  B_SCONS = 30,
   // bf16 stages [NST]: K landed, V landed, V fixed up, stage free.
   B_RFULL = 28,
   B_VFULL = 36,
@@ -240,7 +248,8 @@ __device__ __forceinline__ void dq_store(const DqRaw<D>& r, unsigned char* buf, 
 #pragma unroll
   for (int jb = 0; jb < NBH; ++jb) {
     const int b = hf * NBH + jb;                  // block index in the row
-    const int boff = (b >> 1) * (kNT * 128);
+    // K (with lo parts): 64-d column blocks of hi rows then lo rows.
+    const int boff = (b >> 1) * (lobuf ? 2 : 1) * (kNT * 128);
     const int o = SH + 34 * jb;                   // block offset in the loaded bytes
     dq_block_store(r.w, o >> 2, o & 2, live, buf + boff, lobuf ? lobuf + boff : nullptr, t,
                    (b & 1) * 4);
@@ -312,7 +321,8 @@ __device__ __forceinline__ void dequant_inplace(unsigned char* buf, unsigned cha
 #pragma unroll
   for (int jb = 0; jb < NBH; ++jb) {
     const int b = hf * NBH + jb;                 // block index in the row
-    const int boff = (b >> 1) * (kNT * 128);
+    // K (with lo parts): 64-d column blocks of hi rows then lo rows.
+    const int boff = (b >> 1) * (lobuf ? 2 : 1) * (kNT * 128);
     const int o = sh + 34 * jb;                  // block offset in the thread's words
     if (work)
       dq_block_store(w, o >> 2, o & 2, live, buf + boff, lobuf ? lobuf + boff : nullptr, t,
@@ -419,12 +429,17 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   // Shared-memory regions.
-  //   Q8: tile buffers K0 V0 K1 V1 (raw Q8 rows land at the start of a
-  //       buffer and are dequantised in place: fp16 hi parts of K, V), then
-  //       K-lo tiles L0 L1 (the residual parts of K0, K1).
+  //   Q8: buffers (K_j, V_j), j < NB16, then the P tile.  Raw Q8 rows
+  //       land at the start of a K or V tile and are dequantised in place.
+  //       A K tile holds, per 64-d column block, the 64 token rows of hi
+  //       parts and then the 64 rows of lo parts, so that [hi; lo] is one
+  //       128-row B operand; a V tile is the fp16 values.  The P tile
+  //       holds the fp16 probabilities of a tile, 128 rows of 64 tokens
+  //       (K-major, 128-byte swizzle), the A operand of the P.V MMA.
   //   bf16: stages of (K tile, V tile).
-  auto q8buf = [&](int kv, int j) { return sm + (2 * j + kv) * C::TILE; };
-  auto q8lo = [&](int j) { return sm + (2 * C::NB16 + j) * C::TILE; };
+  auto q8buf = [&](int kv, int j) { return sm + (3 * j + 2 * kv) * C::TILE; };
+  auto q8lo = [&](int j) { return q8buf(0, j) + kNT * 128; };
+  auto q8p = [&]() { return sm + 3 * C::NB16 * C::TILE; };
   auto kst = [&](int st) { return sm + st * 2 * C::TILE; };            // bf16 K stage
   auto vst = [&](int st) { return sm + st * 2 * C::TILE + C::TILE; };  // bf16 V stage
   // L2 prefetch of the raw Q8 rows of tensor kv (0 = K, 1 = V), tile i.
@@ -481,12 +496,11 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
   };
   const bool early = Q8 && p.page_size == 0 && !err && ntiles > 0;
   constexpr int kQRow = D * 2 + 16;
-  // Q staging: the K-lo tiles L0 L1 when the block's rows fit there, else
-  // V1 L0 L1.  K-lo writes always wait until Q is in TMEM; the raw copies
-  // only in the second case, from tile 1 (buffer V1) on.
-  const int qslot = (min(kM, R - rb * kM) * kQRow <= 2 * C::TILE) ? 2 * C::NB16 : 2 * C::NB16 - 1;
-  unsigned char* const qstage = sm + qslot * C::TILE;
-  const int qfirst = qslot == 2 * C::NB16 ? INT_MAX : 1;  // first tile whose raw buffers hold it
+  // Q staging: buffer 1 (K1 V1, 3 tiles, room for 128 rows at every D), so
+  // tile 1's copies and conversions wait until Q is in TMEM.
+  static_assert(kM * kQRow <= 3 * C::TILE, "Q staging");
+  unsigned char* const qstage = q8buf(0, 1);
+  const int qfirst = 1;  // first tile whose buffers hold the staging
 
   if (tid == 0) {
     err_s = 0;
@@ -507,6 +521,8 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
         mbar_init(bar(B_QREADY8 + i), C::DQ_WARPS / 2);
         mbar_init(bar(B_QEMPTY + i), 1);
       }
+      mbar_init(bar(B_PFREE), 1);
+      mbar_init(bar(B_SCONS), 8);
     } else {
       for (int i = 0; i < C::NST; ++i) {
         mbar_init(bar(B_RFULL + i), 1);
@@ -521,9 +537,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
   // Q8: warps 2.. stage this CTA's Q rows in shared memory (rows padded to
   // kQRow bytes so that the lanes of a warp read distinct bank groups) with
   // every load in flight, overlapping the rest of the prologue; the softmax
-  // warps convert them into TMEM.  The staging takes the K-lo tiles when the
-  // block's rows fit there (every raw copy then goes out as soon as its
-  // buffer is free), else V1 onwards; see qslot.
+  // warps convert them into TMEM.  The staging takes buffer 1 (see qstage).
   if (Q8 && warp >= 2) {
     constexpr int CPR = D / 8;  // 16-byte chunks per row
     constexpr int NTHR = C::THREADS - 64;
@@ -690,41 +704,45 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ S issuer
-    // S(i) = Q K_i^T into S buffer i & 1, once K_i is ready and the P.V that
-    // last read that buffer (tile i - 2, whose P it held) has completed.
+    // bf16: S(i) = Q K_i^T into S buffer i & 1, once K_i is ready and the
+    // P.V that last read that buffer (tile i - 2, whose P it held) has
+    // completed.  Q8: one 128-column S buffer; per K step one MMA over the
+    // 128 B rows [K_i hi; K_i lo], so columns 0..63 get Q.K_hi and 64..127
+    // Q.K_lo (the softmax adds them: hi + lo = d*q exactly), once K_i is
+    // ready and the softmax has read S(i - 1).
     if (lane == 0) {
-      constexpr uint32_t ID_QK = idesc_f16(kM, kNT, !Q8, false);
+      constexpr uint32_t ID_QK = idesc_f16(kM, Q8 ? 2 * kNT : kNT, !Q8, false);
       bool ok = mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs);
       bool any = false;
       for (int i = 0; i < ntiles && ok; ++i) {
         const int b = i & 1;
-        uint32_t kaddr, kloaddr = 0;
+        uint32_t kaddr;
         if (Q8) {
           const int jb = i % C::NB16;
           ok = mbar_wait(bar(B_QREADY8 + jb), (i / C::NB16) & 1, abort_p, kWaitNs);
           kaddr = smem_u32(q8buf(0, jb));
-          kloaddr = smem_u32(q8lo(jb));
+          if (ok && i >= 1) ok = mbar_wait(bar(B_SCONS), (i - 1) & 1, abort_p, kWaitNs);
         } else {
           const int st = i % C::NST;
           ok = mbar_wait(bar(B_RFULL + st), (i / C::NST) & 1, abort_p, kWaitNs);
           kaddr = smem_u32(kst(st));
+          if (ok && i >= 2)
+            ok = mbar_wait(bar(B_SFREE + b), ((i - 2) >> 1) & 1, abort_p, kWaitNs);
         }
-        if (ok && i >= 2)
-          ok = mbar_wait(bar(B_SFREE + b), ((i - 2) >> 1) & 1, abort_p, kWaitNs);
         if (!ok) break;
         tc_fence_after();
         const uint64_t kd0 = sdesc_sw128(kaddr, 16, 1024);
-        const uint64_t kl0 = sdesc_sw128(kloaddr, 16, 1024);
+        // Column blocks of 64 d: bf16 K tiles kNT rows apart, Q8 K tiles
+        // 2 kNT rows (hi then lo).
+        constexpr int CB = (Q8 ? 2 : 1) * kNT * 128;
+        const uint32_t scol = tm + C::COL_S0 + (Q8 ? 0 : b * kNT);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t step = (uint64_t)(((kk >> 2) * (kNT * 128) + (kk & 3) * 32) >> 4);
-          mma_ts(tm + C::COL_S0 + b * kNT, tm + C::COL_Q + kk * 8, kd0 + step, ID_QK,
-                 kk > 0 ? 1u : 0u);
-          // Q8: the K elements' residual parts (hi + lo = d*q exactly).
-          if (Q8) mma_ts(tm + C::COL_S0 + b * kNT, tm + C::COL_Q + kk * 8, kl0 + step, ID_QK, 1u);
+          const uint64_t step = (uint64_t)(((kk >> 2) * CB + (kk & 3) * 32) >> 4);
+          mma_ts(scol, tm + C::COL_Q + kk * 8, kd0 + step, ID_QK, kk > 0 ? 1u : 0u);
         }
         any = true;
-        mma_commit(bar(B_SFULL + b));
+        mma_commit(bar(B_SFULL + (Q8 ? 0 : b)));
         if (Q8) mma_commit(bar(B_QEMPTY + i % C::NB16));
       }
       if (!ok) fail();
@@ -738,8 +756,10 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     }
   } else if (warp == C::PV_WARP) {
     // ------------------------------------------------------------ P.V issuer
-    // O += P_t V_t once the softmax has written P_t (into S buffer t & 1)
-    // and V_t is ready; its completion frees the S buffer and V_t's buffer.
+    // O += P_t V_t once the softmax has written P_t (bf16: into S buffer
+    // t & 1 in TMEM; Q8: into the P tile in shared memory) and V_t is
+    // ready; its completion frees that S buffer / the P tile and V_t's
+    // buffer.
     if (lane == 0) {
       constexpr uint32_t ID_PV = idesc_f16(kM, D, !Q8, true);
       bool ok = true, any = false;
@@ -762,14 +782,22 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
         // Descriptor of the tile start; each 16-token K step adds 2048 bytes
         // to its start-address field (no carry: shared addresses < 256 KB).
         const uint64_t vd0 = sdesc_sw128(vaddr, kNT * 128, 1024);
+        // Q8: P tile (K-major, one 128-byte row of 64 tokens per query
+        // row); a 16-token K step is 32 bytes along the row.
+        const uint64_t pd0 = sdesc_sw128(smem_u32(q8p()), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < kNT / 16; ++kk) {
           const uint64_t vd = vd0 + (uint64_t)((kk * 2048) >> 4);
-          mma_ts(tm + C::COL_O, scol + kk * 8, vd, ID_PV, (t > 0 || kk > 0) ? 1u : 0u);
-          if (!Q8) mma_ts(tm + C::COL_O, scol + kNT / 2 + kk * 8, vd, ID_PV, 1u);
+          if (Q8) {
+            mma_ss(tm + C::COL_O, pd0 + (uint64_t)((kk * 32) >> 4), vd, ID_PV,
+                   (t > 0 || kk > 0) ? 1u : 0u);
+          } else {
+            mma_ts(tm + C::COL_O, scol + kk * 8, vd, ID_PV, (t > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tm + C::COL_O, scol + kNT / 2 + kk * 8, vd, ID_PV, 1u);
+          }
         }
         any = true;
-        mma_commit(bar(B_SFREE + bt));
+        mma_commit(bar(Q8 ? B_PFREE : B_SFREE + bt));
         if (Q8) mma_commit(bar(B_QEMPTY + 3 + t % C::NB16));
         else mma_commit(bar(B_REMPTY + t % C::NST));
       }
@@ -865,10 +893,11 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     // arriving there (skipping the work) until the loop ends.
     for (int i = 0; i < ntiles; ++i) {
       const int b = i & 1;
-      if (ok && !__all_sync(0xffffffffu, mbar_wait(bar(B_SFULL + b), (i >> 1) & 1, abort_p, kWaitNs)))
+      if (ok && !__all_sync(0xffffffffu, mbar_wait(bar(B_SFULL + (Q8 ? 0 : b)),
+                                                   Q8 ? (i & 1) : ((i >> 1) & 1), abort_p, kWaitNs)))
         ok = false;
       tc_fence_after();
-      const uint32_t scol = tm + lane_base + C::COL_S0 + b * kNT;
+      const uint32_t scol = tm + lane_base + C::COL_S0 + (Q8 ? 0 : b * kNT);
       const int t0 = slo + i * kNT + 32 * half;  // first token of this half
       const bool plain = (slo + i * kNT + kNT <= ctx) && (slo + i * kNT + kNT <= shi);
       float sv[32];
@@ -876,7 +905,17 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       if (ok && warp_live) {
         uint32_t sr[32];
         tmem_ld32(scol + 32 * half, sr);
-        tmem_wait_ld();
+        if (Q8) {
+          // S = Q.K_hi + Q.K_lo: the lo columns sit kNT further on.
+          uint32_t sl[32];
+          tmem_ld32(scol + kNT + 32 * half, sl);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            sr[c] = __float_as_uint(__uint_as_float(sr[c]) + __uint_as_float(sl[c]));
+        } else {
+          tmem_wait_ld();
+        }
         if (plain && rvalid) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
@@ -893,6 +932,12 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
           }
         }
       }
+      if (Q8) {
+        // S(i) is in registers: the S issuer may overwrite the buffer.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_SCONS));
+      }
       // Row maximum over both halves (raw scores; c_r > 0).
       red_max[b][half][r] = mx;
       named_barrier_sync(5 + quad, 64);  // the row's two halves
@@ -901,8 +946,10 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       const bool need = rvalid && (m_use != -INFINITY) && (mt > m_use + 8.f);
       const float m_new = (m_use == -INFINITY || need) ? mt : m_use;
       if (ok && __any_sync(0xffffffffu, need) &&
-          !__all_sync(0xffffffffu, mbar_wait(bar(B_SFREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1,
-                                             abort_p, kWaitNs)))
+          !__all_sync(0xffffffffu,
+                      Q8 ? mbar_wait(bar(B_PFREE), (i - 1) & 1, abort_p, kWaitNs)
+                         : mbar_wait(bar(B_SFREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_p,
+                                     kWaitNs)))
         ok = false;
       if (ok && __any_sync(0xffffffffu, need)) {
         // Rescale this half of the warp's O rows once the previous P.V landed.
@@ -944,10 +991,27 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
           }
         }
         if (rvalid) l_run += lsum;
-        tmem_st16(scol + 16 * half, ph);
-        if (!Q8) tmem_st16(scol + kNT / 2 + 16 * half, pl);
-        tmem_wait_st();
+        if (Q8) {
+          // P(i) into the P tile once the P.V of tile i - 1 has read it:
+          // this row's 32 tokens are chunks 4 half .. 4 half + 3 of its
+          // 128-byte row.
+          if (i >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar(B_PFREE), (i - 1) & 1, abort_p,
+                                                           kWaitNs)))
+            ok = false;
+          if (ok) {
+            unsigned char* prow = q8p();
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              *reinterpret_cast<uint4*>(prow + sw128_off(r, 4 * half + c)) =
+                  make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
+          }
+        } else {
+          tmem_st16(scol + 16 * half, ph);
+          tmem_st16(scol + kNT / 2 + 16 * half, pl);
+          tmem_wait_st();
+        }
       }
+      if (Q8) fence_proxy_async_smem();  // P tile writes -> the MMA's reads
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL + b));
@@ -1032,13 +1096,10 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
           const int lo_i = i == 0 ? 1 : i + kPrefetch, hi_i = min(i + kPrefetch + 1, ntiles);
           for (int k = lo_i; k < hi_i; ++k) prefetch_q8(k, grp);
         }
-        // K writes its lo tiles, which the Q staging shares, so K always
-        // waits for Q to be in TMEM (once; later waits return at once).
         if (ok && !__all_sync(0xffffffffu,
                               mbar_wait(bar(B_QEMPTY + 3 * grp + jb), ((i / C::NB16) & 1) ^ 1,
                                         abort_p, kWaitNs) &&
-                                  ((grp == 1 && i < qfirst) ||
-                                   mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs)))) {
+                                  (i < qfirst || mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs)))) {
           ok = false;
           if (lane == 0) fail();
         }
@@ -1061,11 +1122,8 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       bool ok = true;
       for (int i = 0; i < ntiles; ++i) {
         const int jb = i % C::NB16;
-        // K also waits for Q to be in TMEM: its lo tiles share the staging.
         if (ok && !__all_sync(0xffffffffu, mbar_wait(bar(B_QFULL + 3 * grp + jb),
-                                                     (i / C::NB16) & 1, abort_p, kWaitNs) &&
-                                               (grp == 1 ||
-                                                mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs)))) {
+                                                     (i / C::NB16) & 1, abort_p, kWaitNs))) {
           ok = false;
           if (lane == 0) fail();
         }
