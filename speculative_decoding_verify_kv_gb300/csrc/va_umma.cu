@@ -196,6 +196,39 @@ __device__ __forceinline__ void dq_block_store(const uint32_t* w, int wo, bool o
   }
 }
 
+// Convert and store the NBH blocks of a half-row held in words w (the first
+// block starting sh = 0 or 2 bytes into w[0]).  K (with lo parts): 64-d
+// column blocks of hi rows then lo rows.  With sh = 0 and an even NBH the
+// blocks go two at a time (68 bytes = 17 words: blocks at words 0 and 8 + 2
+// bytes), the next pair's words moving down by 17 after each step, so the
+// conversion is one two-block step in the code rather than NBH unrolled
+// copies (which would crowd the instruction cache).
+template <int NBH, int NW>
+__device__ __forceinline__ void dq_half_row(uint32_t (&w)[NW], int sh, int hf, bool live,
+                                            unsigned char* buf, unsigned char* lobuf, int t) {
+  if (NBH % 2 == 0 && sh == 0) {
+#pragma unroll 1
+    for (int jp = 0; jp < NBH / 2; ++jp) {
+      const int b0 = hf * NBH + 2 * jp;  // even block index in the row: chunks 0-3, then 4-7
+      const int boff = (b0 >> 1) * (lobuf ? 2 : 1) * (kNT * 128);
+      unsigned char* lo = lobuf ? lobuf + boff : nullptr;
+      dq_block_store(w, 0, false, live, buf + boff, lo, t, 0);
+      dq_block_store(w, 8, true, live, buf + boff, lo, t, 4);
+#pragma unroll
+      for (int q = 0; q + 17 < NW; ++q) w[q] = w[q + 17];
+    }
+  } else {
+#pragma unroll
+    for (int jb = 0; jb < NBH; ++jb) {
+      const int b = hf * NBH + jb;  // block index in the row
+      const int boff = (b >> 1) * (lobuf ? 2 : 1) * (kNT * 128);
+      const int o = sh + 34 * jb;   // block offset in the words
+      dq_block_store(w, o >> 2, o & 2, live, buf + boff, lobuf ? lobuf + boff : nullptr, t,
+                     (b & 1) * 4);
+    }
+  }
+}
+
 // Q8_0 dequantisation by direct loads (paged caches).  A thread owns one
 // half-row (token t = gtid % 64 of the tile, half hf = gtid / 64 of its
 // D/32 blocks).  It loads the raw bytes of its half-row from global memory
@@ -209,10 +242,12 @@ struct DqRaw {
   static constexpr int NB = D / 32;               // blocks per row
   static constexpr int RB = NB * 34;              // bytes per row
   static constexpr int HB = RB / 2;               // bytes per half-row
-  // D = 256: nine 16-byte loads per half, the second half starting 8 bytes
-  // early (both stay inside the row).  Otherwise: 4-byte loads from the word
-  // at or below the first byte.
-  static constexpr int NW = D == 256 ? 36 : (HB + (HB % 4 ? 2 : 0) + 3) / 4;
+  // Does the second half-row start 2 bytes into a word (D = 64 only)?  Else
+  // both halves' blocks sit at the same word offsets, so one conversion
+  // serves both (a second copy of the unrolled conversion would crowd the
+  // instruction cache).
+  static constexpr bool kOdd = (HB % 4) != 0;
+  static constexpr int NW = (HB + (kOdd ? 2 : 0) + 3) / 4;
   uint32_t w[NW];
 };
 
@@ -222,14 +257,34 @@ __device__ __forceinline__ void dq_load(DqRaw<D>& r, const unsigned char* row, i
   using R = DqRaw<D>;
   if (!live) return;
   if (D == 256) {
-    const uint4* q = reinterpret_cast<const uint4*>(row + (hf ? R::HB - 8 : 0));
+    // 136 bytes from an 8-byte boundary: eight 16-byte loads and one 8-byte
+    // load at the end (first half) or at the start (second half).
+    static_assert(D != 256 || R::NW == 34, "D = 256 half-row words");
+    const uint4* q = reinterpret_cast<const uint4*>(row + (hf ? R::HB + 8 : 0));
+    const uint2 e = __ldg(reinterpret_cast<const uint2*>(row + (hf ? R::HB : 128)));
+    uint4 v[8];
 #pragma unroll
-    for (int k = 0; k < 9; ++k) {
-      const uint4 v = __ldg(q + k);
-      r.w[4 * k] = v.x;
-      r.w[4 * k + 1] = v.y;
-      r.w[4 * k + 2] = v.z;
-      r.w[4 * k + 3] = v.w;
+    for (int k = 0; k < 8; ++k) v[k] = __ldg(q + k);
+    if (hf) {
+      r.w[0] = e.x;
+      r.w[1] = e.y;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        r.w[2 + 4 * k] = v[k].x;
+        r.w[3 + 4 * k] = v[k].y;
+        r.w[4 + 4 * k] = v[k].z;
+        r.w[5 + 4 * k] = v[k].w;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        r.w[4 * k] = v[k].x;
+        r.w[1 + 4 * k] = v[k].y;
+        r.w[2 + 4 * k] = v[k].z;
+        r.w[3 + 4 * k] = v[k].w;
+      }
+      r.w[32] = e.x;
+      r.w[33] = e.y;
     }
   } else {
     const int start = hf * R::HB;
@@ -239,35 +294,13 @@ __device__ __forceinline__ void dq_load(DqRaw<D>& r, const unsigned char* row, i
   }
 }
 
-// Convert and store; SH = byte offset of the half-row's first block within
-// the loaded words.
-template <int D, int SH>
-__device__ __forceinline__ void dq_store(const DqRaw<D>& r, unsigned char* buf, unsigned char* lobuf,
-                                         int t, int hf, bool live) {
-  constexpr int NBH = D / 64;                     // blocks per half-row
-#pragma unroll
-  for (int jb = 0; jb < NBH; ++jb) {
-    const int b = hf * NBH + jb;                  // block index in the row
-    // K (with lo parts): 64-d column blocks of hi rows then lo rows.
-    const int boff = (b >> 1) * (lobuf ? 2 : 1) * (kNT * 128);
-    const int o = SH + 34 * jb;                   // block offset in the loaded bytes
-    dq_block_store(r.w, o >> 2, o & 2, live, buf + boff, lobuf ? lobuf + boff : nullptr, t,
-                   (b & 1) * 4);
-  }
-}
-
+// Convert and store a loaded half-row (its words are consumed).
 template <int D>
-__device__ __forceinline__ void dq_convert(const DqRaw<D>& r, unsigned char* buf,
-                                           unsigned char* lobuf, int t, int hf, bool live) {
-  if (D == 256) {
-    if (hf) dq_store<D, 8>(r, buf, lobuf, t, hf, live);
-    else dq_store<D, 0>(r, buf, lobuf, t, hf, live);
-  } else {
-    // 4-byte loads: the half-row starts 0 or 2 bytes into the first word.
-    const int sh = (hf * DqRaw<D>::HB) & 3;
-    if (sh) dq_store<D, 2>(r, buf, lobuf, t, hf, live);
-    else dq_store<D, 0>(r, buf, lobuf, t, hf, live);
-  }
+__device__ __forceinline__ void dq_convert(DqRaw<D>& r, unsigned char* buf, unsigned char* lobuf,
+                                           int t, int hf, bool live) {
+  // The half-row starts 0 bytes into the loaded words, or 2 (second half at
+  // D = 64).
+  dq_half_row<D / 64>(r.w, DqRaw<D>::kOdd && hf ? 2 : 0, hf, live, buf, lobuf, t);
 }
 
 // Dequantise, in place, the raw Q8_0 rows (RB bytes apart) at the start of
@@ -287,7 +320,9 @@ __device__ __forceinline__ void dequant_inplace(unsigned char* buf, unsigned cha
   constexpr int NW = (HB + 2 + 3) / 4 + 1;
   const int t = tid & 63, hf = tid >> 6;
   const int start = t * RB + hf * HB;
-  const int sh = start & 3;       // 0 or 2
+  // 0 or 2; 0 unless HB is not a multiple of 4 (D = 64), which leaves one
+  // unrolled conversion in the code instead of two.
+  const int sh = HB % 4 ? (start & 3) : 0;
   uint32_t w[NW];
   const bool live = work && t < valid;
   if (live) {
@@ -318,16 +353,7 @@ __device__ __forceinline__ void dequant_inplace(unsigned char* buf, unsigned cha
     }
   }
   named_barrier_sync(barid, 128);
-#pragma unroll
-  for (int jb = 0; jb < NBH; ++jb) {
-    const int b = hf * NBH + jb;                 // block index in the row
-    // K (with lo parts): 64-d column blocks of hi rows then lo rows.
-    const int boff = (b >> 1) * (lobuf ? 2 : 1) * (kNT * 128);
-    const int o = sh + 34 * jb;                  // block offset in the thread's words
-    if (work)
-      dq_block_store(w, o >> 2, o & 2, live, buf + boff, lobuf ? lobuf + boff : nullptr, t,
-                     (b & 1) * 4);
-  }
+  if (work) dq_half_row<NBH, NW>(w, sh, hf, live, buf, lobuf, t);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -442,24 +468,18 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
   auto q8p = [&]() { return sm + 3 * C::NB16 * C::TILE; };
   auto kst = [&](int st) { return sm + st * 2 * C::TILE; };            // bf16 K stage
   auto vst = [&](int st) { return sm + st * 2 * C::TILE + C::TILE; };  // bf16 V stage
-  // L2 prefetch of the raw Q8 rows of tensor kv (0 = K, 1 = V), tile i.
+  // Contiguous Q8 cache: L2 prefetch of the raw rows of tensor kv (0 = K,
+  // 1 = V), tile i.
   auto prefetch_q8 = [&](int i, int kv) {
     const unsigned char* src = (const unsigned char*)(kv ? p.v : p.k);
     const int tp = slo + i * kNT;
     const int np = min(tp + kNT, (shi + kPage - 1) / kPage * kPage) - tp;
-    if (p.page_size == 0) {
-      const long long rowp = ((long long)s * p.KVH + kvh) * p.capacity + tp;
-      bulk_prefetch_l2(src + rowp * C::RB, (uint32_t)(np * C::RB));
-    } else {
-      const int ncache = (scratch ? min(np, ctx - tp) : np);  // tokens in the cache
-      for (int pg = 0; pg * kPage < ncache; ++pg) {
-        const int blk = p.block_table[(long long)s * p.max_blocks + tp / kPage + pg];
-        bulk_prefetch_l2(src + ((long long)blk * p.KVH + kvh) * kPage * C::RB, kPage * C::RB);
-      }
-    }
+    const long long rowp = ((long long)s * p.KVH + kvh) * p.capacity + tp;
+    bulk_prefetch_l2(src + rowp * C::RB, (uint32_t)(np * C::RB));
   };
-  // Copy the raw Q8 rows of tensor kv, tile i, into buffer i % NB16 (whose
-  // previous tile must be consumed), and pull tile i + kPrefetch into L2.
+  // Contiguous Q8 cache: copy the raw rows of tensor kv, tile i, into
+  // buffer i % NB16 (whose previous tile must be consumed), and pull tile
+  // i + kPrefetch into L2.
   auto issue_q8 = [&](int i, int kv) {
     const int jb = i % C::NB16;
     const uint64_t pol = policy_evict_first();
@@ -470,16 +490,8 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     const uint32_t fb = bar(B_QFULL + 3 * kv + jb);
     if (i + kPrefetch < ntiles) prefetch_q8(i + kPrefetch, kv);
     mbar_arrive_expect_tx(fb, (uint32_t)(nload * C::RB));
-    if (p.page_size == 0) {
-      const long long rowi = ((long long)s * p.KVH + kvh) * p.capacity + t0;
-      bulk_g2s(smem_u32(dst), src + rowi * C::RB, (uint32_t)(nload * C::RB), fb, pol);
-    } else {
-      for (int pg = 0; pg < nload / kPage; ++pg) {
-        const int blk = p.block_table[(long long)s * p.max_blocks + t0 / kPage + pg];
-        const long long rowi = ((long long)blk * p.KVH + kvh) * kPage;
-        bulk_g2s(smem_u32(dst + pg * kPage * C::RB), src + rowi * C::RB, kPage * C::RB, fb, pol);
-      }
-    }
+    const long long rowi = ((long long)s * p.KVH + kvh) * p.capacity + t0;
+    bulk_g2s(smem_u32(dst), src + rowi * C::RB, (uint32_t)(nload * C::RB), fb, pol);
   };
 
   // Q8, contiguous cache: the raw rows of a tile arrive by one bulk copy per
@@ -1075,6 +1087,32 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       const int t = gtid & 63, hf = gtid >> 6;
       const unsigned char* src = reinterpret_cast<const unsigned char*>(grp ? p.v : p.k);
       const unsigned char* dsrc = reinterpret_cast<const unsigned char*>(grp ? p.dv : p.dk);
+      // Block-table lookups are issued a tile ahead of their use, so that
+      // neither a row's address nor an L2 prefetch waits on one.
+      auto row_blk = [&](int i) {
+        const int tok = slo + i * kNT + t;
+        return tok < shi && !(scratch && tok >= ctx)
+                   ? p.block_table[(long long)s * p.max_blocks + tok / kPage]
+                   : 0;
+      };
+      // L2 prefetch of page pg of tile k (pages holding cache tokens only;
+      // their blocks were checked in the prologue): the block, then the copy.
+      const int cend = scratch ? min(shi, ctx) : shi;
+      auto pf_blk = [&](int k, int pg) {
+        const int tp = slo + k * kNT + pg * kPage;
+        return k < ntiles && tp < cend ? p.block_table[(long long)s * p.max_blocks + tp / kPage] : -1;
+      };
+      auto pf_issue = [&](int blk) {
+        if (blk >= 0) bulk_prefetch_l2(src + ((long long)blk * p.KVH + kvh) * kPage * C::RB, kPage * C::RB);
+      };
+      // Lanes of the group's first warp keep its tensor kPrefetch tiles
+      // ahead in L2, one page each: tiles 1..kPrefetch (16 lanes) before the
+      // first conversion, then tile i + kPrefetch (4 lanes) after converting
+      // tile i.
+      const bool pf_warp = (dq & 3) == 0;
+      static_assert(kNT == 4 * kPage && 4 * kPrefetch <= 32, "prefetch lanes");
+      if (pf_warp && lane < 4 * kPrefetch) pf_issue(pf_blk(1 + lane / 4, lane % 4));
+      int blk_next = row_blk(0);
       // A failed wait does not leave the loop (no named barrier here, but
       // the stores must stay out of buffers an MMA may still read).
       bool ok = true;
@@ -1084,18 +1122,14 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
         const int tok = t0 + t;
         const bool live = ok && tok < shi;
         const bool draft = scratch && tok >= ctx;  // from the tree scratch KV
-        const int blk = live && !draft ? p.block_table[(long long)s * p.max_blocks + tok / kPage] : 0;
+        const int blk = blk_next;
         const unsigned char* row =
             draft ? dsrc + scratch_row(p, row0, kvh, tok - ctx) * C::RB
                   : src + (((long long)blk * p.KVH + kvh) * kPage + tok % kPage) * C::RB;
         DqRaw<D> raw;
         dq_load<D>(raw, row, hf, live);
-        // The group's first thread keeps its tensor kPrefetch tiles ahead in
-        // L2 (tiles 1..kPrefetch once tile 0's reads are out).
-        if (gtid == 0) {
-          const int lo_i = i == 0 ? 1 : i + kPrefetch, hi_i = min(i + kPrefetch + 1, ntiles);
-          for (int k = lo_i; k < hi_i; ++k) prefetch_q8(k, grp);
-        }
+        if (i + 1 < ntiles) blk_next = row_blk(i + 1);
+        const int pfb = pf_warp && lane < 4 && i >= 1 ? pf_blk(i + kPrefetch, lane) : -1;
         if (ok && !__all_sync(0xffffffffu,
                               mbar_wait(bar(B_QEMPTY + 3 * grp + jb), ((i / C::NB16) & 1) ^ 1,
                                         abort_p, kWaitNs) &&
@@ -1108,6 +1142,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_QREADY8 + 3 * grp + jb));
+        pf_issue(pfb);
       }
     } else if (Q8 && dq_slot(warp) >= 0) {
       // The K and V dequantisation groups (dq_slot) each convert their
