@@ -134,6 +134,35 @@ __device__ __forceinline__ bool draft_visible(int kind, unsigned anc, int j, int
   return kind == 0 ? a <= j : ((anc >> a) & 1u) != 0u;
 }
 
+// Bits c of [lo, hi) intersected with [0, 32).
+__device__ __forceinline__ unsigned bit_range(int lo, int hi) {
+  lo = max(lo, 0);
+  hi = min(hi, 32);
+  if (lo >= hi) return 0u;
+  const unsigned up = hi == 32 ? 0xFFFFFFFFu : (1u << hi) - 1u;
+  return up & ~((1u << lo) - 1u);
+}
+
+// Visibility of the 32 tokens t0 .. t0 + 31 of a span [., shi) to local row
+// j of a sequence with ctx context tokens, as bits: context tokens, and
+// draft tokens ctx + a for which draft_visible(kind, anc, j, a) holds.  The
+// same decision as draft_visible token by token, in a few word operations.
+__device__ __forceinline__ unsigned visible_bits(int kind, unsigned anc, int j, int ctx, int shi,
+                                                 int t0) {
+  unsigned m = bit_range(0, min(ctx, shi) - t0);
+  if (shi > ctx) {
+    unsigned dm = bit_range(ctx - t0, shi - t0);
+    if (kind == 0) {
+      dm &= bit_range(ctx - t0, ctx + j + 1 - t0);  // a <= j
+    } else {
+      const int sh = t0 - ctx;  // bit c of the window is draft position c + sh
+      dm &= sh >= 0 ? (sh < 32 ? anc >> sh : 0u) : (-sh < 32 ? anc << -sh : 0u);
+    }
+    m |= dm;
+  }
+  return m;
+}
+
 // Row of token t of (sequence s, KV head kvh), counted in rows of the k/v
 // array; -1 when the block table entry is out of range.
 __device__ __forceinline__ long long kv_row(const Params& p, int s, int kvh, int t) {

@@ -935,11 +935,10 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
             mx = fmaxf(mx, sv[c]);
           }
         } else {
+          const unsigned vis = rvalid ? visible_bits(kind, anc, j, ctx, shi, t0) : 0u;
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const int t = t0 + c;
-            const bool vis = rvalid && t < shi && (t < ctx || draft_visible(kind, anc, j, t - ctx));
-            sv[c] = vis ? __uint_as_float(sr[c]) : -INFINITY;
+            sv[c] = (vis >> c) & 1u ? __uint_as_float(sr[c]) : -INFINITY;
             mx = fmaxf(mx, sv[c]);
           }
         }
@@ -983,24 +982,16 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       if (ok && warp_live) {
         uint32_t ph[16], pl[16];
         float lsum = 0.f;
-        const float mneg = -m_use;
-        if (plain) {
+        // A masked score (-inf) gives 2^-inf = 0.  m_use is finite once any
+        // score of the row was visible; while none was, every score here is
+        // masked and the 0 offset keeps -inf * c_r + offset at -inf.
+        const float mneg = m_use == -INFINITY ? 0.f : -m_use;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float a = ex2_approx(fmaf(sv[2 * c], c_r, mneg));
-            const float bb = ex2_approx(fmaf(sv[2 * c + 1], c_r, mneg));
-            lsum += a + bb;
-            pack_p<Q8>(a, bb, ph[c], pl[c]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float a = sv[2 * c] == -INFINITY ? 0.f : ex2_approx(fmaf(sv[2 * c], c_r, mneg));
-            const float bb =
-                sv[2 * c + 1] == -INFINITY ? 0.f : ex2_approx(fmaf(sv[2 * c + 1], c_r, mneg));
-            lsum += a + bb;
-            pack_p<Q8>(a, bb, ph[c], pl[c]);
-          }
+        for (int c = 0; c < 16; ++c) {
+          const float a = ex2_approx(fmaf(sv[2 * c], c_r, mneg));
+          const float bb = ex2_approx(fmaf(sv[2 * c + 1], c_r, mneg));
+          lsum += a + bb;
+          pack_p<Q8>(a, bb, ph[c], pl[c]);
         }
         if (rvalid) l_run += lsum;
         if (Q8) {
