@@ -134,10 +134,14 @@ typedef struct va_kv {
  *   Query head h reads KV head h / (num_heads / num_kv_heads).
  *   scale: softmax scale; 0 selects 1/sqrt(head_dim).
  *   num_splits: S >= 1.  Sequence s's span L = ctx + n is cut into chunks
- *      of max(ceil(L/T), 128) tokens rounded up to a whole number of
- *      64-token tiles (at most T chunks), where T (>= S, <= 16 S) is fixed
- *      by S, num_kv_heads and the GPU's SM count only (one wave of CTAs per
- *      sequence and KV head); each chunk writes an fp32 online-softmax
+ *      of max(ceil(L/Ts), 128) tokens rounded up to a whole number of
+ *      64-token tiles (at most Ts chunks).  T (>= S, <= 16 S) is fixed by S,
+ *      num_kv_heads and the GPU's SM count only (one wave of CTAs per
+ *      sequence and KV head); a sequence whose n * G query rows span b > 1
+ *      row blocks of the partial kernel (128 rows on the tensor-core
+ *      kernels, 16 on the CUDA-core kernel), each of which reads the span
+ *      again, uses Ts = max(S, floor(T / b)) chunks (T otherwise); each
+ *      chunk writes an fp32 online-softmax
  *      partial and a merge pass combines them in ascending order (hipfire
  *      PR #817, "Summary" and "Performance").  No choice depends on the
  *      other sequences of the launch, so a row's result depends only on
@@ -265,9 +269,10 @@ va_status va_debug_gather_index(const va_problem *p, const va_kv *kv, int32_t kv
  * launch).  For sequence s and slot j < T (T = va_plan's slots),
  * ranges[2*(s*T + j)] and ranges[2*(s*T + j) + 1] are the first and
  * one-past-last KV position of chunk j, computed by the device functions
- * the partial kernels call: with L = ctx_len[s] + rows of s, a chunk has
- * c = max(ceil(L / T), 128) rounded up to a multiple of 64 tokens and
- * chunk j is [min(j c, L), min((j + 1) c, L)) (empty past L).  A sequence
+ * the partial kernels call: with L = ctx_len[s] + rows of s and Ts the
+ * sequence's chunk count (see num_splits), a chunk has c = max(ceil(L / Ts),
+ * 128) rounded up to a multiple of 64 tokens and chunk j is [min(j c, L),
+ * min((j + 1) c, L)) (empty past L; slots Ts .. T - 1 are empty).  A sequence
  * whose row offsets are inconsistent gets -1, -1 and sets
  * VA_DEV_BAD_ROWS.  ranges: device int32[num_seqs * T * 2].
  */

@@ -240,6 +240,18 @@ def device_chunk_count(S: int, num_kv_heads: int, sm_count: int, ctas_per_sm: in
     return max(S, min(T, 16 * S))
 
 
+def device_seq_chunks(T: int, S: int, rows: int, group: int, rows_per_block: int) -> int:
+    """How many of the T chunks the GPU library cuts a sequence with `rows`
+    query rows into: T shared out among the sequence's row blocks (ceil(rows
+    * group / rows_per_block) of them; each streams the span again), but at
+    least S.  A sequence of one row block keeps all T.  rows_per_block is 128
+    for the row-major tensor-core kernel and 16 for the CUDA-core kernel.
+    Like device_chunk_count, the library's reading, not the pages': it
+    depends on the sequence alone."""
+    rb = max(1, -(-rows * group // rows_per_block))
+    return max(S, T // rb)
+
+
 def device_chunk_ranges(L: int, T: int) -> list[tuple[int, int]]:
     """The GPU library's chunks of a span of L tokens cut T ways: chunk
     length c = max(ceil(L / T), 128) rounded up to a multiple of 64 tokens

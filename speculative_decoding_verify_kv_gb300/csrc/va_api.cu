@@ -202,6 +202,7 @@ static Params make_params(const va_problem* p, const va_kv* kv, int mode, const 
   q.P = pl.P;
   q.slots = pl.slots;
   q.min_sub = kMinSubTokens;
+  q.min_splits = p->num_splits;
   q.mode = mode;
   q.kv_dtype = kv->dtype;
   q.q_dtype = p->q_dtype;

@@ -23,6 +23,7 @@ struct Params {
   int total_rows, max_rows;
   int S, P, slots;        // logical splits, sub-chunks per split, S*P
   int min_sub;            // smallest sub-chunk (tokens) before a split is cut further
+  int min_splits;         // the caller's split count: a sequence keeps at least this many chunks
   int mode;               // va_mode
   int kv_dtype, q_dtype;  // va_dtype
   float scale_log2;       // softmax scale * log2(e)
@@ -82,6 +83,16 @@ __device__ __forceinline__ void sub_range(int lo, int hi, int P, int min_sub, in
   long long a = lo + (long long)p * sub, b = lo + (long long)(p + 1) * sub;
   *slo = (int)(a < hi ? a : hi);
   *shi = (int)(b < hi ? b : hi);
+}
+
+// Chunk count of a sequence with n query rows: the launch's count P shared
+// out among the sequence's row blocks (each row block streams the span
+// again, so a many-row sequence takes fewer, longer chunks), but at least
+// the caller's split count.  It depends on the sequence alone.
+__device__ __forceinline__ int seq_subs(const Params& p, int n) {
+  const int rb = (n * p.G + p.rows_per_block - 1) / p.rows_per_block;
+  const int c = p.P / (rb > 1 ? rb : 1);
+  return c > p.min_splits ? c : p.min_splits;
 }
 
 // Number of non-empty chunks of [lo, hi) under sub_range (they come first).

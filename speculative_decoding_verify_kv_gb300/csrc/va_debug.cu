@@ -52,7 +52,7 @@ __global__ void debug_split_kernel(const Params p, int* ranges) {
     if (!(err & VA_DEV_BAD_ROWS)) {
       int lo, hi;
       split_range(ctx + n, p.S, 0, &lo, &hi);
-      sub_range(lo, hi, p.P, p.min_sub, j, &slo, &shi);
+      sub_range(lo, hi, seq_subs(p, n), p.min_sub, j, &slo, &shi);
     }
     ranges[2 * ((long long)s * p.slots + j)] = slo;
     ranges[2 * ((long long)s * p.slots + j) + 1] = shi;

@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const Params p)
   if (!nan && p.S == 1 && sctx >= 0) {
     int lo0, hi0;
     split_range(sctx + sn, 1, 0, &lo0, &hi0);
-    live = max(1, live_subs(lo0, hi0, p.P, p.min_sub));
+    live = max(1, live_subs(lo0, hi0, seq_subs(p, sn), p.min_sub));
   }
   for (int s0 = grp; s0 < live && !nan; s0 += BATCH * NG) {
     float mm[BATCH], ll[BATCH];

@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_partial_kernel(const Params
 
   int lo, hi, slo, shi;
   split_range(L, p.S, split, &lo, &hi);
-  sub_range(lo, hi, p.P, p.min_sub, sub, &slo, &shi);
+  sub_range(lo, hi, seq_subs(p, n), p.min_sub, sub, &slo, &shi);
 
   // Q rows of this block -> shared (fp32).
   for (int i = tid; i < nrows * D; i += kSimtThreads) {

@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
   const int L = ctx + n;
   int lo, hi, slo, shi;
   split_range(L, p.S, 0, &lo, &hi);
-  sub_range(lo, hi, p.P, p.min_sub, slot, &slo, &shi);
+  sub_range(lo, hi, seq_subs(p, n), p.min_sub, slot, &slo, &shi);
   const int ntiles = (shi - slo + kTT - 1) / kTT;
   if (ntiles == 0 && !err) {
     // An empty chunk (short span): its rows' slots become (-inf, 0) at once,

@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
   const int L = ctx + n;
   int lo, hi, slo, shi;
   split_range(L, p.S, split, &lo, &hi);
-  sub_range(lo, hi, p.P, p.min_sub, sub, &slo, &shi);
+  sub_range(lo, hi, seq_subs(p, n), p.min_sub, sub, &slo, &shi);
   const int ntiles = (shi - slo + kNT - 1) / kNT;
   if (ntiles == 0 && !err) {
     // An empty chunk (short span): its rows' slots become (-inf, 0) at once,

@@ -124,11 +124,16 @@ def check_device_split_golden():
     for c in d["cases"]:
         T = orc.device_chunk_count(c["S"], c["KVH"], c["sms"], c["ctas_per_sm"])
         assert T == c["T"], (c["work"], T)
+        Ts = T
+        if "rows" in c:
+            Ts = orc.device_seq_chunks(T, c["S"], c["rows"], c["G"], c["rows_per_block"])
+            assert Ts == c["Ts"], (c["work"], Ts)
         want = [(j * c["c"], (j + 1) * c["c"]) for j in range(c["full"])]
         if c["tail"] is not None:
             want.append(tuple(c["tail"]))
         want += [(c["L"], c["L"])] * c["empty"]
-        got = orc.device_chunk_ranges(c["L"], T)
+        got = orc.device_chunk_ranges(c["L"], Ts)
+        got += [(c["L"], c["L"])] * (T - Ts)
         assert got == want, (c["work"], got[:3], got[-3:])
 
 

@@ -1,7 +1,9 @@
 """The chunks the GPU kernels run, read back through va_debug_split_ranges
 (the same device functions the partial kernels call) and compared bit for
 bit with the oracle's restatement of the library's chunk rule, which the CPU
-tests pin to hand-worked cases (tests/golden/device_split_plan.json)."""
+tests pin to hand-worked cases (tests/golden/device_split_plan.json): T
+chunks per sequence, of which a sequence spanning several row blocks uses
+fewer, longer ones."""
 import numpy as np
 import pytest
 
@@ -13,6 +15,7 @@ import synthetic as sy
 # Spans L = ctx + 16 rows: the hand-worked lengths plus a short one.
 SPANS = [1024, 1032, 32784, 100, 8208, 16]
 KVH = 4
+ROWS = {va.KERNEL_TENSOR: 128, va.KERNEL_CUDA_CORES: 16}  # query rows per CTA
 
 
 def _case(dtype, S):
@@ -42,8 +45,9 @@ def test_device_chunks_match_the_restated_rule(dtype, flags, ctas, kernel, S):
     assert pl["slots"] == T
     got = va.debug_split_ranges(p, kv, mode).cpu().numpy()
     assert got.shape == (len(SPANS), T, 2)
+    Ts = orc.device_seq_chunks(T, S, 16, 2, ROWS[kernel])
     for s, L in enumerate(SPANS):
-        want = np.array(orc.device_chunk_ranges(L, T), dtype=np.int32)
+        want = np.array(orc.device_chunk_ranges(L, Ts) + [(L, L)] * (T - Ts), dtype=np.int32)
         assert np.array_equal(got[s], want), (L, got[s][:4].tolist(), want[:4].tolist())
 
 
@@ -54,7 +58,7 @@ def test_device_chunks_match_the_hand_worked_cases():
     sms = _sm_count()
     d = P.load("device_split_plan.json")
     cases = [c for c in d["cases"] if c["sms"] == sms and c["ctas_per_sm"] == 1 and c["KVH"] == KVH
-             and c["L"] in SPANS]
+             and c["L"] in SPANS and "rows" not in c]
     if not cases:
         pytest.skip(f"no hand-worked case for {sms} SMs")
     for c in cases:
@@ -79,3 +83,36 @@ def test_chunks_do_not_depend_on_the_other_sequences():
         p1, kv1, mode1 = va.upload(one, "cuda", num_splits=8)
         alone = va.debug_split_ranges(p1, kv1, mode1).cpu().numpy()
         assert np.array_equal(alone[0], full[s])
+
+
+@pytest.mark.gpu
+def test_many_row_sequences_take_fewer_chunks():
+    """Sequences of several row blocks (prefill-sized chains) beside a
+    one-row sequence in one launch: each sequence's chunks follow its own row
+    count (hand-worked cases where the SM count matches, the restated rule
+    always), and the one-row sequence keeps all T."""
+    sms = _sm_count()
+    rows, ctx = [256, 64, 1], [8192, 8384, 8447]   # spans of 8448 tokens
+    case = sy.make_case("split-rows", num_heads=24, num_kv_heads=KVH, head_dim=64, kv_dtype=sy.Q8_0,
+                        q_dtype=sy.BF16, ctx=ctx, rows=rows, seed=43, num_splits=8)
+    p, kv, mode = va.upload(case, "cuda", num_splits=8)
+    pl = va.plan(p, kv, mode)
+    assert pl["kernel"] == va.KERNEL_TENSOR
+    T = orc.device_chunk_count(8, KVH, sms, 1)
+    got = va.debug_split_ranges(p, kv, mode).cpu().numpy()
+    assert got.shape == (3, T, 2)
+    for s in range(3):
+        L = ctx[s] + rows[s]
+        Ts = orc.device_seq_chunks(T, 8, rows[s], 6, ROWS[va.KERNEL_TENSOR])
+        want = orc.device_chunk_ranges(L, Ts) + [(L, L)] * (T - Ts)
+        assert got[s].tolist() == [list(r) for r in want], (s, Ts)
+    assert orc.device_seq_chunks(T, 8, 1, 6, 128) == T
+    d = P.load("device_split_plan.json")
+    for c in d["cases"]:
+        if c.get("rows") in (256, 64) and c["sms"] == sms and c["L"] == 8448 and c["KVH"] == KVH:
+            s = rows.index(c["rows"])
+            want = [(j * c["c"], (j + 1) * c["c"]) for j in range(c["full"])]
+            if c["tail"] is not None:
+                want.append(tuple(c["tail"]))
+            want += [(c["L"], c["L"])] * c["empty"]
+            assert got[s].tolist() == [list(r) for r in want], c["work"]

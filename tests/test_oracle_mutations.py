@@ -83,6 +83,14 @@ def _device_count_unclamped(S, num_kv_heads, sm_count, ctas_per_sm):
     return ctas_per_sm * sm_count // num_kv_heads
 
 
+def _seq_chunks_ignore_rows(T, S, rows, group, rows_per_block):
+    return T
+
+
+def _seq_chunks_no_floor(T, S, rows, group, rows_per_block):
+    return T // max(1, -(-rows * group // rows_per_block))
+
+
 def _merge_no_rescale(parts):
     live = [p for p in parts if p[1] > 0]
     M = max(p[0] for p in live)
@@ -134,7 +142,8 @@ def _span_rows_scratch_shifted(cache, draft, s, kvh, ctx, n, lo, **kw):
 _orig = {name: getattr(orc, name) for name in
          ["attend", "visible_positions", "ancestors", "kv_head_of", "dequant_q8_0",
           "decode_fp16", "split_ranges", "merge", "gather_index", "promote",
-          "promote_preflight", "span_rows", "device_chunk_ranges", "device_chunk_count"]}
+          "promote_preflight", "span_rows", "device_chunk_ranges", "device_chunk_count",
+          "device_seq_chunks"]}
 
 MUTATIONS = {
     "scale dropped": ("attend", _attend_no_scale),
@@ -155,6 +164,8 @@ MUTATIONS = {
     "device chunks in 16-token steps": ("device_chunk_ranges", _device_chunks_tile16),
     "device chunks without the 128-token minimum": ("device_chunk_ranges", _device_chunks_no_minimum),
     "device chunk count not clamped to [S, 16 S]": ("device_chunk_count", _device_count_unclamped),
+    "sequence chunk count ignores its row blocks": ("device_seq_chunks", _seq_chunks_ignore_rows),
+    "sequence chunk count not floored at S": ("device_seq_chunks", _seq_chunks_no_floor),
 }
 
 
