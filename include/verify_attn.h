@@ -287,9 +287,10 @@ va_status va_debug_split_ranges(const va_problem *p, const va_kv *kv, int32_t mo
 
 typedef struct va_plan_info {
   int32_t kernel;          /* VA_KERNEL_* */
-  int32_t sub_splits;      /* T: KV chunks per sequence (equal to slots) */
+  int32_t sub_splits;      /* T: KV chunks per sequence of one row block (equal to slots) */
   int32_t slots;           /* T partial slots per (row, head) */
-  int32_t grid_x, grid_y, grid_z;
+  int32_t grid_x, grid_y, grid_z; /* x: max(T, S * row blocks of the longest sequence);
+                                     y: KV heads; z: sequences */
   int32_t threads;
   int32_t smem_bytes;
 } va_plan_info;

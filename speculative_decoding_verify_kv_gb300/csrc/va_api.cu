@@ -173,8 +173,12 @@ static Plan make_plan(const va_problem* p, const va_kv* kv) {
   pl.slots = slots;
   const int rows = p->max_rows_per_seq * G;
   pl.row_blocks = (rows + pl.rows_per_block - 1) / pl.rows_per_block;
-  pl.grid = dim3((unsigned)(pl.slots * pl.row_blocks), (unsigned)kv->num_kv_heads,
-                 (unsigned)p->num_seqs);
+  // Per (KV head, sequence) the CTAs of a sequence's row blocks times its
+  // chunks (cta_work): T chunks for a sequence of one row block, max(S,
+  // T / b) for one of b blocks, so max(T, S * row_blocks) CTAs cover all.
+  const int per = pl.slots > p->num_splits * pl.row_blocks ? pl.slots
+                                                           : p->num_splits * pl.row_blocks;
+  pl.grid = dim3((unsigned)per, (unsigned)kv->num_kv_heads, (unsigned)p->num_seqs);
   return pl;
 }
 

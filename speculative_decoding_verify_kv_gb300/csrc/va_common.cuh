@@ -95,6 +95,27 @@ __device__ __forceinline__ int seq_subs(const Params& p, int n) {
   return c > p.min_splits ? c : p.min_splits;
 }
 
+// Work of partial CTA x (blockIdx.x) for a sequence with n query rows: its
+// b row blocks times its seq_subs chunks, laid out chunk-major (x = chunk *
+// b + row block).  The grid holds max(T, S * most row blocks) such CTAs per
+// (KV head, sequence), which covers every sequence; false for x past this
+// sequence's work.  *ts = seq_subs(p, n).
+__device__ __forceinline__ bool cta_work(const Params& p, int n, int x, int* rb, int* chunk,
+                                         int* ts) {
+  const int rows = n * p.G;
+  if (rows <= p.rows_per_block) {
+    *ts = p.P > p.min_splits ? p.P : p.min_splits;
+    *rb = 0;
+    *chunk = x;
+    return x < *ts;
+  }
+  const int b = (rows + p.rows_per_block - 1) / p.rows_per_block;
+  *ts = seq_subs(p, n);
+  *rb = x % b;
+  *chunk = x / b;
+  return *chunk < *ts;
+}
+
 // Number of non-empty chunks of [lo, hi) under sub_range (they come first).
 __device__ __forceinline__ int live_subs(int lo, int hi, int P, int min_sub) {
   const int len = hi - lo;

@@ -48,9 +48,6 @@ __global__ void __launch_bounds__(kSimtThreads) simt_partial_kernel(const Params
   // read or written before that work has completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rb = blockIdx.x % p.row_blocks;
-  const int sp = blockIdx.x / p.row_blocks;
-  const int split = sp / p.P, sub = sp % p.P, slot = sp;
   const int kvh = blockIdx.y, s = blockIdx.z;
 
   int row0, n, ctx;
@@ -59,6 +56,10 @@ __global__ void __launch_bounds__(kSimtThreads) simt_partial_kernel(const Params
     if (tid == 0) flag(p.status, err);
     return;  // the rows of this sequence are unknown
   }
+  // Row block and chunk (one level of chunks: split 0, slot = chunk).
+  int rb, sub, nsub;
+  if (!cta_work(p, n, blockIdx.x, &rb, &sub, &nsub)) return;
+  const int split = 0, slot = sub;
   const int R = n * p.G;
   const int rbase = rb * kSimtRows;
   if (rbase >= R) return;
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_partial_kernel(const Params
 
   int lo, hi, slo, shi;
   split_range(L, p.S, split, &lo, &hi);
-  sub_range(lo, hi, seq_subs(p, n), p.min_sub, sub, &slo, &shi);
+  sub_range(lo, hi, nsub, p.min_sub, sub, &slo, &shi);
 
   // Q rows of this block -> shared (fp32).
   for (int i = tid; i < nrows * D; i += kSimtThreads) {

@@ -246,8 +246,6 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rb = blockIdx.x % p.row_blocks;
-  const int slot = blockIdx.x / p.row_blocks;
   const int kvh = blockIdx.y, s = blockIdx.z;
 
   int row0, n, ctx;
@@ -256,6 +254,8 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
     if (tid == 0) flag(p.status, err);
     return;
   }
+  int rb, slot, nsub;  // row block, chunk, the sequence's chunk count
+  if (!cta_work(p, n, blockIdx.x, &rb, &slot, &nsub)) return;
   const int G = p.G;
   const int R = n * G;
   if (rb * kNR >= R) return;
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(tq8::kThreads, 1)
   const int L = ctx + n;
   int lo, hi, slo, shi;
   split_range(L, p.S, 0, &lo, &hi);
-  sub_range(lo, hi, seq_subs(p, n), p.min_sub, slot, &slo, &shi);
+  sub_range(lo, hi, nsub, p.min_sub, slot, &slo, &shi);
   const int ntiles = (shi - slo + kTT - 1) / kTT;
   if (ntiles == 0 && !err) {
     // An empty chunk (short span): its rows' slots become (-inf, 0) at once,

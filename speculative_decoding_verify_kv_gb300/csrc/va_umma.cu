@@ -402,9 +402,6 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
   // written before that work has completed and its writes are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rb = blockIdx.x % p.row_blocks;
-  const int sp = blockIdx.x / p.row_blocks;
-  const int split = sp / p.P, sub = sp % p.P, slot = sp;
   const int kvh = blockIdx.y, s = blockIdx.z;
 
   int row0, n, ctx;
@@ -413,13 +410,17 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     if (tid == 0) flag(p.status, err);
     return;
   }
+  // Row block and chunk (one level of chunks: split 0, slot = chunk).
+  int rb, sub, nsub;
+  if (!cta_work(p, n, blockIdx.x, &rb, &sub, &nsub)) return;
+  const int split = 0, slot = sub;
   const int G = p.G;
   const int R = n * G;
   if (rb * kM >= R) return;
   const int L = ctx + n;
   int lo, hi, slo, shi;
   split_range(L, p.S, split, &lo, &hi);
-  sub_range(lo, hi, seq_subs(p, n), p.min_sub, sub, &slo, &shi);
+  sub_range(lo, hi, nsub, p.min_sub, sub, &slo, &shi);
   const int ntiles = (shi - slo + kNT - 1) / kNT;
   if (ntiles == 0 && !err) {
     // An empty chunk (short span): its rows' slots become (-inf, 0) at once,

@@ -219,7 +219,8 @@ def test_plan_rule():
     assert plan(q8, num_splits=1)["slots"] == clamp(sms // 4, 1, 16)
     simt = plan(q8, flags=va.FLAG_CUDA_CORES)
     assert simt["kernel"] == va.KERNEL_CUDA_CORES and simt["slots"] == clamp(2 * sms // 4, 8, 128)
-    assert simt["grid_x"] == simt["slots"] * -(-16 * 6 // 16)      # 16-row blocks
+    # grid x: a sequence's row blocks times its chunks, at most max(T, S * blocks)
+    assert simt["grid_x"] == max(simt["slots"], 8 * -(-16 * 6 // 16))   # 16-row blocks
     d128 = sy.make_case("p", num_heads=32, num_kv_heads=8, head_dim=128, kv_dtype=sy.BF16,
                         q_dtype=sy.BF16, ctx=[40, 50], rows=[16, 16], paged=True, seed=1)
     pl = plan(d128, num_splits=8)
@@ -228,10 +229,10 @@ def test_plan_rule():
     long_chain = sy.make_case("c", num_heads=24, num_kv_heads=4, head_dim=256, kv_dtype=sy.Q8_0,
                               q_dtype=sy.BF16, ctx=[40], rows=[100], seed=2)
     pl = plan(long_chain, num_splits=8)
-    assert pl["grid_x"] == pl["slots"] * 5                 # 600 query rows: 5 blocks of 128
+    assert pl["grid_x"] == max(pl["slots"], 8 * 5)         # 600 query rows: 5 blocks of 128
     bf_chain = sy.make_case("c", num_heads=24, num_kv_heads=4, head_dim=256, kv_dtype=sy.BF16,
                             q_dtype=sy.BF16, ctx=[40], rows=[100], seed=2)
-    assert plan(bf_chain, num_splits=8)["grid_x"] == pl["slots"] * 5   # blocks of 128
+    assert plan(bf_chain, num_splits=8)["grid_x"] == max(pl["slots"], 8 * 5)   # blocks of 128
     f32 = sy.tiny_chain()
     assert plan(f32)["kernel"] == va.KERNEL_CUDA_CORES
     mixed = sy.mixed_tree_direct(ctx=[40, 300, 17, 130], direct=(0, 2), num_splits=2, seed=7)
