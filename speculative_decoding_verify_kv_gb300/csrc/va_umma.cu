@@ -495,6 +495,23 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     bulk_g2s(smem_u32(dst), src + rowi * C::RB, (uint32_t)(nload * C::RB), fb, pol);
   };
 
+  // bf16, contiguous cache: tile i's K and V by tiled TMA loads (one per
+  // 64-d column block) into stage i % NST.
+  auto issue_bf16 = [&](int i) {
+    const int st = i % C::NST;
+    const uint64_t pol = policy_evict_first();
+    const int t0 = slo + i * kNT;
+    mbar_arrive_expect_tx(bar(B_RFULL + st), (uint32_t)C::TILE);
+    mbar_arrive_expect_tx(bar(B_VFULL + st), (uint32_t)C::TILE);
+    const int plane = s * p.KVH + kvh;
+    for (int db = 0; db < C::DBLK; ++db) {
+      tma_load_3d(smem_u32(kst(st) + db * kNT * 128), &tmK, db * 64, t0, plane, bar(B_RFULL + st),
+                  pol);
+      tma_load_3d(smem_u32(vst(st) + db * kNT * 128), &tmV, db * 64, t0, plane, bar(B_VFULL + st),
+                  pol);
+    }
+  };
+
   // Q8, contiguous cache: the raw rows of a tile arrive by one bulk copy per
   // tensor into the tile buffer and are dequantised in place.  Paged cache:
   // a tile would take one small copy per 16-token page, so the dequantising
@@ -503,11 +520,16 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
   // range (the span was checked against the capacity), so these copies go
   // out before the rest of the prologue.
   constexpr bool direct = Q8 && PAGED;
+  // bf16, contiguous cache: likewise tile 0's tensor loads (stage 0).
   auto issue_first = [&]() {
-    issue_q8(0, 0);
-    issue_q8(0, 1);
+    if (Q8) {
+      issue_q8(0, 0);
+      issue_q8(0, 1);
+    } else {
+      issue_bf16(0);
+    }
   };
-  const bool early = Q8 && p.page_size == 0 && !err && ntiles > 0;
+  const bool early = p.page_size == 0 && !err && ntiles > 0;
   constexpr int kQRow = D * 2 + 16;
   // Q staging: buffer 1 (K1 V1, 3 tiles, room for 128 rows at every D), so
   // tile 1's copies and conversions wait until Q is in TMEM.
@@ -603,8 +625,8 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       // Let the copies already issued land before the CTA goes away.
       int dummy = 0;
       volatile int* never = &dummy;
-      mbar_wait(bar(B_QFULL), 0, never, kWaitNs);
-      mbar_wait(bar(B_QFULL + 3), 0, never, kWaitNs);
+      mbar_wait(bar(Q8 ? B_QFULL : B_RFULL), 0, never, kWaitNs);
+      mbar_wait(bar(Q8 ? B_QFULL + 3 : B_VFULL), 0, never, kWaitNs);
     }
     if (err && tid == 0) flag(p.status, err);
     if (rvalid) {
@@ -665,7 +687,8 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
           issued = i + 1;
         }
       } else {
-        for (int i = 0; i < ntiles; ++i) {
+        issued = early ? 1 : 0;
+        for (int i = issued; i < ntiles; ++i) {
           const int st = i % C::NST;
           if (!mbar_wait(bar(B_REMPTY + st), ((i / C::NST) & 1) ^ 1, abort_p, kWaitNs)) {
             fail();
@@ -675,15 +698,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
           const int end16 = min(t0 + kNT, (shi + kPage - 1) / kPage * kPage);
           const int nload = end16 - t0;
           if (p.page_size == 0) {
-            mbar_arrive_expect_tx(bar(B_RFULL + st), (uint32_t)C::TILE);
-            mbar_arrive_expect_tx(bar(B_VFULL + st), (uint32_t)C::TILE);
-            const int plane = s * p.KVH + kvh;
-            for (int db = 0; db < C::DBLK; ++db) {
-              tma_load_3d(smem_u32(kst(st) + db * kNT * 128), &tmK, db * 64, t0, plane,
-                          bar(B_RFULL + st), pol);
-              tma_load_3d(smem_u32(vst(st) + db * kNT * 128), &tmV, db * 64, t0, plane,
-                          bar(B_VFULL + st), pol);
-            }
+            issue_bf16(i);
           } else {
             const uint32_t bytes = (uint32_t)(nload * D * 2);
             mbar_arrive_expect_tx(bar(B_RFULL + st), bytes);
@@ -870,11 +885,20 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
         qscale = ldexpf(1.f, -e);
         c_r = ldexpf(p.scale_log2, e);
       }
-#pragma unroll 1
+      // bf16: every load of the half-row in flight at once (one round trip
+      // to global memory); Q8: from shared memory, four at a time.
+      uint4 qa[Q8 ? 1 : NQ];
+      if (!Q8) {
+#pragma unroll
+        for (int k = 0; k < (Q8 ? 1 : NQ); ++k)
+          qa[k] = rvalid ? qsrc[k] : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll (Q8 ? 1 : NQ / 4)
       for (int c = 0; c < NQ / 4; ++c) {
         uint4 q4[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) q4[k] = rvalid ? qsrc[4 * c + k] : make_uint4(0u, 0u, 0u, 0u);
+        for (int k = 0; k < 4; ++k)
+          q4[k] = Q8 ? (rvalid ? qsrc[4 * c + k] : make_uint4(0u, 0u, 0u, 0u)) : qa[(Q8 ? 0 : 4 * c + k)];
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
