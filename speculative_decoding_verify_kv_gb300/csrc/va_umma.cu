@@ -533,8 +533,11 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
   constexpr int kQRow = D * 2 + 16;
   // Q staging: buffer 1 (K1 V1, 3 tiles, room for 128 rows at every D), so
   // tile 1's copies and conversions wait until Q is in TMEM.
-  static_assert(kM * kQRow <= 3 * C::TILE, "Q staging");
-  unsigned char* const qstage = q8buf(0, 1);
+  // bf16: from stage 1 on (stages 1 and 2 at most), so tile 1's loads
+  // wait likewise.
+  static_assert(!Q8 || kM * kQRow <= 3 * C::TILE, "Q staging");
+  static_assert(Q8 || kM * kQRow <= (C::NST - 1) * 2 * C::TILE, "Q staging");
+  unsigned char* const qstage = Q8 ? q8buf(0, 1) : kst(1);
   const int qfirst = 1;  // first tile whose buffers hold the staging
 
   if (tid == 0) {
@@ -569,11 +572,13 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     fence_barrier_init();
     if (early) issue_first();
   }
-  // Q8: warps 2.. stage this CTA's Q rows in shared memory (rows padded to
+  // Warps 2.. stage this CTA's Q rows in shared memory (rows padded to
   // kQRow bytes so that the lanes of a warp read distinct bank groups) with
-  // every load in flight, overlapping the rest of the prologue; the softmax
-  // warps convert them into TMEM.  The staging takes buffer 1 (see qstage).
-  if (Q8 && warp >= 2) {
+  // every load in flight and consecutive lanes on consecutive 16 bytes of a
+  // row, overlapping the rest of the prologue; the softmax warps move them
+  // into TMEM (Q8: converted to fp16).  The staging takes buffer 1 / stage
+  // 1 on (see qstage).
+  if (warp >= 2) {
     constexpr int CPR = D / 8;  // 16-byte chunks per row
     constexpr int NTHR = C::THREADS - 64;
     constexpr int ITER = (kM * CPR + NTHR - 1) / NTHR;
@@ -690,7 +695,10 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
         issued = early ? 1 : 0;
         for (int i = issued; i < ntiles; ++i) {
           const int st = i % C::NST;
-          if (!mbar_wait(bar(B_REMPTY + st), ((i / C::NST) & 1) ^ 1, abort_p, kWaitNs)) {
+          // The stages of tiles qfirst.. hold the Q staging until the
+          // softmax warps have put Q into TMEM.
+          if ((i == qfirst && !mbar_wait(bar(B_QREADY), 0, abort_p, kWaitNs)) ||
+              !mbar_wait(bar(B_REMPTY + st), ((i / C::NST) & 1) ^ 1, abort_p, kWaitNs)) {
             fail();
             break;
           }
@@ -856,12 +864,9 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       // rescale of the whole row (exact), the 2^e folded into the score
       // multiplier; the two halves exchange their |q| maxima.
       constexpr int NQ = D / 16;  // uint4 per half row
-      // Q8: from the shared staging copy (rows padded so the lanes of a warp
-      // hit distinct bank groups); bf16: straight from global memory.
-      const uint4* qsrc =
-          Q8 ? reinterpret_cast<const uint4*>(qstage + r * kQRow + half * D)
-             : reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned short*>(p.q) +
-                                              ((long long)grow * p.H + h) * D + half * (D / 2));
+      // From the shared staging copy (rows padded so the lanes of a warp
+      // hit distinct bank groups).
+      const uint4* qsrc = reinterpret_cast<const uint4*>(qstage + r * kQRow + half * D);
       float qscale = 1.f;
       if (Q8) {
         float amax = 0.f;
@@ -885,20 +890,11 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
         qscale = ldexpf(1.f, -e);
         c_r = ldexpf(p.scale_log2, e);
       }
-      // bf16: every load of the half-row in flight at once (one round trip
-      // to global memory); Q8: from shared memory, four at a time.
-      uint4 qa[Q8 ? 1 : NQ];
-      if (!Q8) {
-#pragma unroll
-        for (int k = 0; k < (Q8 ? 1 : NQ); ++k)
-          qa[k] = rvalid ? qsrc[k] : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll (Q8 ? 1 : NQ / 4)
+#pragma unroll 1
       for (int c = 0; c < NQ / 4; ++c) {
         uint4 q4[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          q4[k] = Q8 ? (rvalid ? qsrc[4 * c + k] : make_uint4(0u, 0u, 0u, 0u)) : qa[(Q8 ? 0 : 4 * c + k)];
+        for (int k = 0; k < 4; ++k) q4[k] = rvalid ? qsrc[4 * c + k] : make_uint4(0u, 0u, 0u, 0u);
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
