@@ -83,8 +83,8 @@ def parse():
 # sources (comments and white space aside) are the ones it was taken on.
 PROFILED_TRAFFIC = {
     "kernel": 1,
-    "bytes": 73_608_960,
-    "sources": {"va_umma.cu": "afe5758c7f365b37", "va_common.cuh": "1ee9aa830ce21a73",
+    "bytes": 72_948_224,
+    "sources": {"va_umma.cu": "564ac4aa45c6838c", "va_common.cuh": "c2688452ae35bd94",
                 "va_sm100.cuh": "ff735fa02c94f492"},
 }
 
