@@ -8,13 +8,18 @@
 // tile:
 //
 //   S = Q K^T      tcgen05.mma, A = Q (TMEM), B = K tile (smem, K-major);
-//                  Q8: one MMA for K's fp16 hi parts and one for its lo
-//                  parts per K step
+//                  bf16: N = 64 tokens into one of two S buffers; Q8: N =
+//                  128 over [K hi rows; K lo rows] of the tile, one MMA per
+//                  K step, into one S buffer (columns 0..63 Q.K_hi, 64..127
+//                  Q.K_lo)
 //   softmax        8 warps, one TMEM lane (= query row) per thread and one
 //                  half of the tile's columns per warp; masks (chain rows
 //                  causal by index, tree rows by ancestor mask); online
-//                  (m, l) in log2 units; P written back over S
-//   O += P V       tcgen05.mma, A = P (TMEM), B = V tile (smem, MN-major)
+//                  (m, l) in log2 units; P written back over S (bf16) or
+//                  into a shared-memory P tile (Q8, after the softmax has
+//                  released the S buffer)
+//   O += P V       tcgen05.mma, A = P (TMEM for bf16, the shared P tile for
+//                  Q8), B = V tile (smem, MN-major)
 //
 // O (fp32, 128 lanes x D columns) lives in TMEM for the CTA's whole range.
 // At the end each row's (m, l, O) goes to its partial slot; the merge
@@ -26,17 +31,20 @@
 //     copy per tensor into a tile buffer; four warps per tensor dequantise
 //     them in place to fp16 in the 128-byte-swizzled MMA layout,
 //     zero-filling tokens past the range.  A K element d*q (up to 18
-//     significant bits) becomes hi = fp16(d*q) in place and the residual
-//     lo = fma(d, q, -hi), exact in fp16, in a K-lo tile, so the two S MMAs
-//     see d*q exactly; V elements are fp16(d*q) (one rounding).  Paged (a separate
+//     significant bits) becomes hi = fp16(d*q) and the residual lo =
+//     fma(d, q, -hi), exact in fp16, written 64 rows below it in the same
+//     column block, so the S MMA over [hi; lo] sees d*q exactly; V
+//     elements are fp16(d*q) (one rounding).  Paged (a separate
 //     instantiation): the same warps load the raw rows themselves through
 //     the block table (a tree sequence's drafts from the tree scratch KV
-//     when one is given).  Q is converted to fp16 after a per-row power-of-two
-//     rescale (exact), and the scale folds into the score multiplier.  P
-//     is fp16.
+//     when one is given).  Q is converted to fp16 after a per-row
+//     power-of-two rescale (exact), and the scale folds into the score
+//     multiplier.  P is fp16.
 //   bf16: tiled TMA loads place K/V tiles directly in the MMA layout; one
 //     warp zeroes V rows past the range of a ragged tile.  P is split into
 //     bf16 hi + lo halves (two MMAs) so P keeps 16 significant bits.
+//   Both: Q rows are staged in shared memory by warps 2.. with coalesced
+//     loads during the prologue and moved into TMEM by the softmax warps.
 //
 // Warp roles: 0 = copy producer, 1 = TMEM owner + S MMA issuer, 2..9 =
 // softmax/epilogue (two warps per TMEM lane quadrant), 13 (Q8) or 11
