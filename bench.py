@@ -70,7 +70,8 @@ def parse():
                          "(--ctx selects the context), no graphs, no JSON line")
     ap.add_argument("--ctx", type=int, default=HEADLINE_CTX)
     ap.add_argument("--workload", default="long-q8",
-                    choices=["long-q8", "mixed-tree-direct", "paged-d128-q8", "dflash-bf16"],
+                    choices=["long-q8", "mixed-tree-direct", "paged-d128-q8", "paged-d128-bf16",
+                             "dflash-bf16"],
                     help="--profile only: the workload whose calls are run (--ctx applies to "
                          "long-q8 and dflash-bf16)")
     return ap.parse_args()
@@ -674,6 +675,7 @@ def run_profile(args):
     case = {"long-q8": lambda: sy.long_q8(ctx=args.ctx, num_splits=SPLITS),
             "mixed-tree-direct": lambda: sy.mixed_tree_direct(),
             "paged-d128-q8": lambda: sy.paged_d128(kv_dtype=sy.Q8_0),
+            "paged-d128-bf16": lambda: sy.paged_d128(),
             "dflash-bf16": lambda: sy.dflash_bf16(ctx=args.ctx, num_splits=SPLITS)}[args.workload]()
     l2 = int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2 ** 20))
     b = Bench(case, flags, l2)
