@@ -385,9 +385,9 @@ __device__ __forceinline__ void pack_p(float a, float b, uint32_t& hi, uint32_t&
   }
 }
 
-// PAGED (Q8 only): the cache is paged and the dequantising warps load the
-// raw rows themselves; a separate instantiation, so the contiguous kernel
-// carries none of that code.
+// PAGED: the cache is paged (Q8: the dequantising warps load the raw rows
+// themselves; bf16: one tensor load per 16-token page); a separate
+// instantiation, so the contiguous kernel carries none of that code.
 template <int D, int KVT, bool PAGED>
 __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D, KVT>::MAXREG))
     umma_partial_kernel(const Params p, const __grid_constant__ CUtensorMap tmK,
@@ -537,7 +537,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
       issue_bf16(0);
     }
   };
-  const bool early = p.page_size == 0 && !err && ntiles > 0;
+  const bool early = !PAGED && !err && ntiles > 0;
   constexpr int kQRow = D * 2 + 16;
   // Q staging: buffer 1 (K1 V1, 3 tiles, room for 128 rows at every D), so
   // tile 1's copies and conversions wait until Q is in TMEM.
@@ -618,7 +618,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
     anc = row_mask(kind, p.parent + row0, j, &bad);
     if (bad) atomicOr(&err_s, (int)VA_DEV_BAD_PARENT);
   }
-  if (!err && p.page_size != 0 && ntiles > 0) {
+  if (PAGED && !err && ntiles > 0) {
     const int cend = scratch ? min(shi, ctx) : shi;  // cache tokens of the range
     const int pg0 = slo / kPage, pg1 = (cend + kPage - 1) / kPage;
     for (int pg = pg0 + tid; pg < pg1; pg += blockDim.x) {
@@ -713,7 +713,7 @@ __global__ void __launch_bounds__(UCfg<D, KVT>::THREADS, 1) __maxnreg__((UCfg<D,
           const int t0 = slo + i * kNT;
           const int end16 = min(t0 + kNT, (shi + kPage - 1) / kPage * kPage);
           const int nload = end16 - t0;
-          if (p.page_size == 0) {
+          if (!PAGED) {
             issue_bf16(i);
           } else {
             const uint32_t bytes = (uint32_t)(nload * D * 2);
@@ -1318,8 +1318,10 @@ int umma_smem_bytes(int D, int kv_dtype) {
 }
 
 cudaError_t launch_umma_partial(const Params& p, dim3 grid, cudaStream_t st) {
-#define VA_U_BF16(DD) \
-  if (p.D == DD && p.kv_dtype == VA_BF16) return launch_umma_t<DD, VA_BF16, false>(p, grid, st);
+#define VA_U_BF16(DD)                                                                     \
+  if (p.D == DD && p.kv_dtype == VA_BF16)                                                 \
+    return p.page_size != 0 ? launch_umma_t<DD, VA_BF16, true>(p, grid, st)              \
+                            : launch_umma_t<DD, VA_BF16, false>(p, grid, st);
 #define VA_U_Q8(DD)                                                                       \
   if (p.D == DD && p.kv_dtype == VA_Q8_0)                                                 \
     return p.page_size != 0 ? launch_umma_t<DD, VA_Q8_0, true>(p, grid, st)              \
