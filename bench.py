@@ -84,8 +84,8 @@ def parse():
 # sources (comments and white space aside) are the ones it was taken on.
 PROFILED_TRAFFIC = {
     "kernel": 1,
-    "bytes": 72_948_224,
-    "sources": {"va_umma.cu": "564ac4aa45c6838c", "va_common.cuh": "c2688452ae35bd94",
+    "bytes": 73_136_640,
+    "sources": {"va_umma.cu": "721253357a9ab7ec", "va_common.cuh": "c2688452ae35bd94",
                 "va_sm100.cuh": "ff735fa02c94f492"},
 }
 
